@@ -1,0 +1,475 @@
+#!/usr/bin/env python
+"""Benchmark of the TurboQuant KV-cache hot path on one GB300 (or N replicas).
+
+One step = the whole hot path on one batch: the fused store of each
+sequence's newest token (tq_store) followed by split-K decode attention over
+the packed paged cache (tq_decode_attention: stage 1 + stage 2).  Default
+workload: Llama-3-8B-shaped decode (B=32, 32 q / 8 kv heads, head_dim 128,
+8192-token contexts, block_size 16, preset turboquant_k8v4, bf16, random
+block-table permutation), synthetic seeded data.
+
+Prints ONE JSON line (rank 0).  `value` is packed-KV bytes read per step
+divided by the device-timed step (GB/s), summed over ranks; `e2e` is the same
+metric with every step's inputs copied from pinned host memory and the
+attention output copied back, inside the timed region.
+
+--impl reference times the CPU oracle (the slow plain-C definition of the
+method) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_kv_cache_04_gb300 import workloads as wl  # noqa: E402
+
+SLOT = {"turboquant_k8v4": 196, "turboquant_4bit_nc": 134, "turboquant_k3v4_nc": 118,
+        "turboquant_3bit_nc": 102}
+L2_BYTES = 129 * 2**20
+NOMINAL_HBM_GBS = 8000.0
+
+
+def _args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="llama3_8b",
+                   choices=["llama3_8b", "qwen3_32b", "long", "store_mixed", "sweep", "tiny"])
+    p.add_argument("--preset", default=None, choices=sorted(SLOT))
+    p.add_argument("--ctx", type=int, default=None)
+    p.add_argument("--batch", type=int, default=None)
+    p.add_argument("--splits", type=int, default=None, help="0 = library picks")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true", help="skip the store-throughput side run")
+    return p.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _describe(w) -> str:
+    ctx = (f"ctx {int(w.seq_lens[0])}" if len(set(w.seq_lens.tolist())) == 1
+           else f"ctx {int(w.seq_lens.min())}-{int(w.seq_lens.max())}")
+    return (f"{w.name} decode: B={w.B}, Hq={w.Hq}, Hk={w.Hk}, D={w.D}, {ctx}, "
+            f"bs {w.block_size}, {w.preset}, {w.dtype}")
+
+
+def _kv_bytes(w) -> int:
+    return int(w.seq_lens.astype(np.int64).sum()) * w.Hk * SLOT[w.preset]
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows, self.proc, self.err = [], None, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception as e:  # pragma: no cover
+            self.err = str(e)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # pragma: no cover
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.err or "no nvidia-smi samples"}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    it was taken on is the one being timed (else null)."""
+    src = os.path.join(ROOT, "quantized_kv_cache_04_gb300", "csrc", "tq_decode.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    f = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(f):
+        return None
+    for line in open(f):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == workload \
+                and parts[1] == kernel and parts[2] == sha:
+            return float(parts[3])
+    return None
+
+
+# ---------------------------------------------------------------- GPU setup
+class Problem:
+    """Device-resident cache, queries and per-step inputs of one workload."""
+
+    def __init__(self, w, dev, splits):
+        import torch
+        import quantized_kv_cache_04_gb300 as tq
+        self.w, self.dev = w, dev
+        self.c = tq.TQCache(w.preset, w.num_blocks, w.block_size, w.Hk, device=dev)
+        self.c.cache[w.guard_block] = 0xFF          # never read if paging is right
+        CH = 32768
+        for b in range(w.B):
+            n = int(w.seq_lens[b])
+            for t0 in range(0, n, CH):
+                t1 = min(n, t0 + CH)
+                K, V = wl.gen_kv(w, b, t0, t1, dev)
+                sm = torch.from_numpy(w.slot_mapping(b, np.arange(t0, t1))).to(dev)
+                self.c.store(K, V, sm)
+        # the step's new token of every sequence: its last position
+        nk, nv = [], []
+        for b in range(w.B):
+            n = int(w.seq_lens[b])
+            K, V = wl.gen_kv(w, b, n - 1, n, dev)
+            nk.append(K[0])
+            nv.append(V[0])
+        self.new_k = torch.stack(nk).contiguous()
+        self.new_v = torch.stack(nv).contiguous()
+        last = np.array([w.slot_mapping(b, [int(w.seq_lens[b]) - 1])[0] for b in range(w.B)],
+                        np.int64)
+        self.new_sm = torch.from_numpy(last).to(dev)
+        self.q = wl.gen_q(w, dev).contiguous()
+        self.bt = torch.from_numpy(w.block_table).to(dev)
+        self.sl = torch.from_numpy(w.seq_lens).to(dev)
+        self.max_len = int(w.seq_lens.max())
+        self.S = (splits if splits else w.num_splits) or tq.tq_decode_pick_splits(
+            w.B, w.Hq, w.Hk, self.max_len)
+        self.ws = self.c.workspace(w.B, w.Hq, self.S)
+        self.out = torch.empty((w.B, w.Hq, w.D), dtype=self.q.dtype, device=dev)
+        self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+
+    def store(self):
+        self.c.store(self.new_k, self.new_v, self.new_sm)
+
+    def decode(self):
+        self.c.decode(self.q, self.bt, self.sl, self.max_len, self.out, self.lse, self.ws,
+                      num_splits=self.S)
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_device(p: Problem, steps: int, warmup: int, world: int, gpu_index: int):
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        p.store()
+        p.decode()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        e0.record(st)
+        for i in range(steps):
+            p.store()
+            ev[i][0].record(st)
+            p.decode()
+            ev[i][1].record(st)
+        e1.record(st)
+        torch.cuda.synchronize()
+    _barrier(world)
+    total_ms = e0.elapsed_time(e1)
+    dec = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, float(np.mean(dec)), clk.summary()
+
+
+def time_e2e(p: Problem, steps: int, warmup: int, world: int):
+    """Same step with host inputs: pinned H2D of q, new K/V, slot mapping,
+    block table and seq_lens, then D2H of the attention output and LSE."""
+    import torch
+    st = torch.cuda.current_stream()
+    hq = p.q.cpu().pin_memory()
+    hk, hv = p.new_k.cpu().pin_memory(), p.new_v.cpu().pin_memory()
+    hsm = p.new_sm.cpu().pin_memory()
+    hbt, hsl = p.bt.cpu().pin_memory(), p.sl.cpu().pin_memory()
+    hout = torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory()
+    hlse = torch.empty(p.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hsm, hbt, hsl))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
+
+    def step():
+        p.q.copy_(hq, non_blocking=True)
+        p.new_k.copy_(hk, non_blocking=True)
+        p.new_v.copy_(hv, non_blocking=True)
+        p.new_sm.copy_(hsm, non_blocking=True)
+        p.bt.copy_(hbt, non_blocking=True)
+        p.sl.copy_(hsl, non_blocking=True)
+        p.store()
+        p.decode()
+        hout.copy_(p.out, non_blocking=True)
+        hlse.copy_(p.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0.record(st)
+    for _ in range(steps):
+        step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    _barrier(world)
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def time_store_mixed(dev):
+    """Store throughput side run: 16384 new tokens of 16 varlen sequences,
+    bs 32, 8 kv heads, every preset in turn (fp16 inputs)."""
+    import torch
+    import quantized_kv_cache_04_gb300 as tq
+    res = {}
+    for preset in SLOT:
+        w = wl.make("store_mixed", preset=preset)
+        ks, vs, sms = [], [], []
+        for b in range(w.B):
+            n = int(w.seq_lens[b])
+            K, V = wl.gen_kv(w, b, 0, n, dev)
+            ks.append(K)
+            vs.append(V)
+            sms.append(w.slot_mapping(b, np.arange(n)))
+        K, V = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+        sm = torch.from_numpy(np.concatenate(sms)).to(dev)
+        c = tq.TQCache(preset, w.num_blocks, w.block_size, w.Hk, device=dev)
+        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+        for _ in range(5):
+            c.store(K, V, sm)
+        ts = []
+        for _ in range(30):
+            flush.zero_()                           # evict L2 between runs
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            c.store(K, V, sm)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = float(np.median(ts))
+        N = K.shape[0]
+        moved = N * w.Hk * (2 * 2 * w.D + SLOT[preset]) + 8 * N
+        res[preset] = {"tokens": N, "ms": round(ms, 4), "mtok_s": round(N / ms / 1e3, 2),
+                       "gbs": round(moved / ms / 1e6, 1)}
+    return res
+
+
+# ---------------------------------------------------------------- oracle timing
+def _oracle_sample(w, tokens: int, seq: int = 0):
+    """Oracle cache for the first `tokens` positions of sequence `seq` (all kv
+    heads), built by the oracle from CPU-drawn inputs of the same workload."""
+    import oracle as orc
+    n = min(tokens, int(w.seq_lens[seq]))
+    K, V = wl.gen_kv(w, seq, 0, n, "cpu")
+    lay = orc.layout(w.preset_id)
+    s = orc.signs(w.D, 42)
+    c32, m32 = ((np.zeros(1, np.float32),) * 2 if lay["key_fp8"]
+                else orc.codebook(w.D, lay["key_bits"]))
+    bs = w.block_size
+    nb = (n + bs - 1) // bs
+    cache = np.zeros((nb, bs, w.Hk, lay["slot_size_aligned"]), np.uint8)
+    t0 = time.perf_counter()
+    orc.store(w.preset_id, K.float().numpy(), V.float().numpy(), np.arange(n, dtype=np.int64),
+              cache, bs, s, c32, m32)
+    store_s = time.perf_counter() - t0
+    bt = np.arange(nb, dtype=np.int32)[None, :]
+    q = wl.gen_q(w, "cpu")[seq:seq + 1].float().numpy()
+    return dict(n=n, cache=cache, bt=bt, q=q, s=s, c32=c32, store_s=store_s,
+                bytes=n * w.Hk * SLOT[w.preset])
+
+
+def _oracle_decode_once(w, smp):
+    import oracle as orc
+    t0 = time.perf_counter()
+    orc.decode_dense(w.preset_id, smp["q"], smp["cache"], smp["bt"],
+                     np.array([smp["n"]], np.int32), w.Hk, w.block_size, smp["s"], smp["c32"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget_s: float = 10.0):
+    tokens = 256
+    smp = _oracle_sample(w, tokens)
+    t = _oracle_decode_once(w, smp)
+    # grow the sample to about budget_s of oracle decode work (one sequence)
+    tokens = int(min(int(w.seq_lens[0]), max(256, tokens * budget_s / max(t, 1e-6))))
+    smp = _oracle_sample(w, tokens)
+    t = _oracle_decode_once(w, smp)
+    return {"value": round(smp["bytes"] / t / 1e9, 6), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (f"sequence 0, first {smp['n']} tokens, all {w.Hk} kv heads, "
+                       f"{w.Hq // w.Hk} q heads each: dense fp64 decode over the oracle's cache "
+                       f"({t:.1f} s); oracle store of the same tokens took {smp['store_s']:.1f} s"),
+            "store_tok_s": round(smp["n"] / smp["store_s"], 1)}
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the CPU oracle timed on the host cores, each step one
+    decode of a bounded sample of the workload (rank 0 only)."""
+    if rank != 0:
+        return
+    probe = _oracle_sample(w, 256)
+    t = _oracle_decode_once(w, probe)
+    budget = 120.0 / max(1, args.steps + args.warmup)     # whole run ~2 minutes
+    tokens = int(min(int(w.seq_lens[0]), max(16, 256 * budget / max(t, 1e-6))))
+    smp = _oracle_sample(w, tokens)
+    for _ in range(args.warmup):
+        _oracle_decode_once(w, smp)
+    ts = [_oracle_decode_once(w, smp) for _ in range(args.steps)]
+    step_s = float(np.mean(ts))
+    val = smp["bytes"] / step_s / 1e9
+    sample = (f"sequence 0, first {smp['n']} tokens x {w.Hk} kv heads x {w.Hq // w.Hk} q heads "
+              f"per step: dense fp64 oracle decode over the oracle's cache")
+    print(json.dumps({
+        "impl": "reference", "metric": "decode-attn HBM GB/s on packed KV", "value": round(val, 6),
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _describe(w), "sample_tokens": smp["n"]},
+        "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main():
+    args = _args()
+    rank, world, local = _dist()
+    w = wl.make(args.workload, preset=args.preset, ctx=args.ctx, batch=args.batch)
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    import torch
+    assert torch.cuda.is_available(), "bench.py --impl ours needs a CUDA device"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import quantized_kv_cache_04_gb300 as tq
+    tq.load(build_if_missing=True)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+
+    p = Problem(w, dev, args.splits)
+    assert args.warmup >= 3
+    total_ms, dec_ms, clocks = time_device(p, args.steps, args.warmup, world, gpu_index)
+    step_ms = _max_over_ranks(total_ms / args.steps, world)
+    dec_ms = _max_over_ranks(dec_ms, world)
+    kvb = _kv_bytes(w)
+    value = world * kvb / (step_ms * 1e-3) / 1e9
+
+    e2e_steps = args.e2e_steps or max(10, min(args.steps, 500))
+    e2e_ms, h2d, d2h = time_e2e(p, e2e_steps, 3, world)
+    e2e_ms = _max_over_ranks(e2e_ms, world)
+    out_ok = bool(torch.isfinite(p.out.float()).all().item())
+
+    peak, peak_kind = _peaks()
+    achieved = kvb / (dec_ms * 1e-3) / 1e9
+    line = {
+        "metric": "decode-attn HBM GB/s on packed KV", "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": _describe(w), "preset": w.preset, "batch": w.B,
+                   "seq_len": int(w.seq_lens.max()), "block_size": w.block_size,
+                   "num_splits": p.S, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": f"inputs larger than L2 ({kvb / 1e6:.0f} MB packed KV > 129 MiB L2)"
+                   if kvb > L2_BYTES else "inputs smaller than L2 (not flushed)"},
+        "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5), "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": _traffic(args.workload, "tq_decode_attention"),
+                     "kernel": "tq_decode_attention (stage1 + stage2), CUDA events per call",
+                     "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "algorithmic_bytes": kvb},
+        "tokens_per_s": round(world * w.B / (step_ms * 1e-3), 1),
+        "kv_tokens_per_s": round(world * int(w.seq_lens.sum()) / (step_ms * 1e-3), 1),
+        "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "decode_ms": round(dec_ms, 5),
+        "output_finite": out_ok,
+    }
+    if not args.no_extra and rank == 0:
+        line["store_mixed"] = time_store_mixed(dev)
+        line["store_mtok_s"] = line["store_mixed"]["turboquant_4bit_nc"]["mtok_s"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

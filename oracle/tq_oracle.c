@@ -243,6 +243,21 @@ void orc_hadamard(int D, double* H)
             H[(size_t)i * D + j] = (orc_popcount((unsigned)(i & j)) & 1) ? -r : r;
 }
 
+/* The matrix for the head dimension in use, built once and kept (the store
+ * and dequant loops would otherwise rebuild it for every slot). */
+static const double* orc_hadamard_cached(int D)
+{
+    static double* H = NULL;
+    static int HD = 0;
+    if (HD != D) {
+        free(H);
+        H = (double*)malloc(sizeof(double) * D * D);
+        orc_hadamard(D, H);
+        HD = D;
+    }
+    return H;
+}
+
 /* ======================================================================
  * Bit packing.  [Atlas] "Background": 3-bit data is 8 values per 3 bytes;
  * 4-bit is two per byte, 2-bit four per byte.  Bit order is not given on
@@ -349,8 +364,7 @@ int orc_store_one(int preset, int D, const float* k, const float* v,
         double n2 = 0.0;
         for (int i = 0; i < D; ++i) n2 += (double)k[i] * (double)k[i];
         double n = sqrt(n2);
-        double* H = (double*)malloc(sizeof(double) * D * D);
-        orc_hadamard(D, H);
+        const double* H = orc_hadamard_cached(D);
         int* idx = (int*)malloc(sizeof(int) * D);
         double cn2 = 0.0;
         for (int i = 0; i < D; ++i) {
@@ -367,7 +381,7 @@ int orc_store_one(int preset, int D, const float* k, const float* v,
         double norm = L.norm_correction ? n / sqrt(cn2) : n;
         orc_pack(idx, D, L.key_bits, slot);
         orc_put_u16(slot + L.off_k_norm, orc_double_to_f16(norm));
-        free(H); free(idx);
+        free(idx);
     }
     orc_store_values(&L, D, v, slot);
     return 0;
@@ -419,14 +433,12 @@ int orc_dequant_slot(int preset, int D, const uint8_t* slot,
         } else {
             double norm = orc_f16_to_double(orc_get_u16(slot + L.off_k_norm));
             orc_unpack(slot, D, L.key_bits, codes);
-            double* H = (double*)malloc(sizeof(double) * D * D);
-            orc_hadamard(D, H);
+            const double* H = orc_hadamard_cached(D);
             for (int i = 0; i < D; ++i) {
                 double r = 0.0;
                 for (int j = 0; j < D; ++j) r += H[(size_t)i * D + j] * (double)c32[codes[j]];
                 k_hat[i] = norm * signs[i] * r;
             }
-            free(H);
         }
     }
     if (v_hat) {

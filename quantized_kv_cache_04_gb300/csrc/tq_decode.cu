@@ -1,0 +1,316 @@
+// Split-K decode attention read straight from the compressed paged cache.
+//
+// Method: "vllm-project/vllm pull 38479" digest, implementation item 4 (stage 1
+// scores from the compressed cache and accumulates values per split, stage 2
+// merges splits by log-sum-exp); "vllm.v1.attention.backends.turboquant_attn"
+// API page, section "_decode_attention" (GQA grouping, fixed split count,
+// shared mid_o / lse scratch); "turboquant-plus.md", "weight pre-rotation"
+// note (<Q H, H K> = <Q, K>, so q is rotated once and keys stay rotated).
+//
+// This file holds the CUDA-core path: one CTA per (split, kv head, sequence),
+// four warps striding over the split's tokens, 4 coordinates per lane, fp32
+// scores and online softmax, partials merged across warps in shared memory.
+#include "tq.h"
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+#include <cmath>
+
+namespace tq {
+
+int pick_splits(int batch, int num_kv_heads, int max_seq_len)
+{
+    if (batch <= 0 || num_kv_heads <= 0 || max_seq_len <= 0) return 1;
+    const long long units = (long long)batch * num_kv_heads;
+    long long s = (4LL * kNumSMs + units - 1) / units;           // ~4 CTAs per SM
+    const long long by_len = (max_seq_len + 255) / 256;          // >= 256 tokens per split
+    if (s > by_len) s = by_len;
+    if (s < 1) s = 1;
+    if (s > TQ_MAX_SPLITS) s = TQ_MAX_SPLITS;
+    return int(s);
+}
+
+namespace {
+
+struct DecodeArgs {
+    const void* query;
+    const uint8_t* cache;
+    long long num_blocks;
+    const int32_t* block_table;
+    int bt_stride;
+    const int32_t* seq_lens;
+    float scale;
+    int num_splits;
+    const int8_t* signs;
+    const float* centroids;
+    float* mid;          // (B, Hq, S, D+1)
+    void* out;
+    float* lse;
+    int B, Hq, Hk, G, bs;
+    SlotGeom g;
+};
+
+constexpr int kWarps = 4;
+
+// Codes 4*lane .. 4*lane+3 of a BITS-wide LSB-first stream starting at p.
+template <int BITS>
+__device__ __forceinline__ void load_codes(const uint8_t* p, int lane, int (&c)[4])
+{
+    uint32_t w;
+    if constexpr (BITS == 4) {
+        w = ld_u16(p + 2 * lane);
+    } else {
+        static_assert(BITS == 3, "3 or 4 bits");
+        const int bit = 12 * lane;
+        const uint8_t* q = p + (bit >> 3);
+        w = (uint32_t(q[0]) | uint32_t(q[1]) << 8) >> (bit & 7);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (w >> (BITS * i)) & ((1u << BITS) - 1);
+}
+
+template <typename TQ, bool KEY_FP8, int KBITS, int VBITS, int GM>
+__global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
+{
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = a.G, S = a.num_splits;
+    const int L = a.seq_lens[b];
+    const int chunk = (L + S - 1) / S;
+    const int t0 = split * chunk;
+    const int t1 = min(L, t0 + chunk);
+
+    __shared__ float s_cent[16];
+    __shared__ float s_m[kWarps][GM], s_l[kWarps][GM];
+    __shared__ float s_acc[kWarps][GM][kHeadDim];
+
+    if (t0 >= t1) {   // empty split: lse = -inf, zero partial output
+        for (int i = threadIdx.x; i < G * (kHeadDim + 1); i += blockDim.x) {
+            const int g = i / (kHeadDim + 1), d = i % (kHeadDim + 1);
+            float* m = a.mid + (((long long)b * a.Hq + h * G + g) * S + split) * (kHeadDim + 1);
+            m[d] = d == kHeadDim ? -INFINITY : 0.f;
+        }
+        return;
+    }
+    if constexpr (!KEY_FP8) {
+        if (threadIdx.x < (1 << KBITS)) s_cent[threadIdx.x] = a.centroids[threadIdx.x];
+    }
+
+    // q (rotated once for MSE keys), pre-multiplied by the softmax scale
+    float qv[GM][4];
+    const TQ* Q = static_cast<const TQ*>(a.query);
+    float sgn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sgn[i] = KEY_FP8 ? 1.f : float(a.signs[4 * lane + i]);
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+        if (g < G) {
+            const TQ* qp = Q + ((long long)b * a.Hq + h * G + g) * kHeadDim + 4 * lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qv[g][i] = sgn[i] * to_f32(qp[i]);
+            if constexpr (!KEY_FP8) {
+                fwht128_warp(qv[g], lane);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qv[g][i] *= 0.08838834764831845f;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qv[g][i] *= a.scale;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qv[g][i] = 0.f;
+        }
+    }
+    __syncthreads();
+
+    float m[GM], l[GM], acc[GM][4];
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[g][i] = 0.f;
+    }
+
+    const int SB = a.g.slot;
+    const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
+    for (int t = t0 + warp; t < t1; t += kWarps) {
+        const long long page = bt[t / a.bs];
+        const uint8_t* sp = a.cache + ((page * a.bs + t % a.bs) * a.Hk + h) * (long long)SB;
+
+        float kv[4];
+        float knorm = 1.f;
+        if constexpr (KEY_FP8) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __half_raw hr = __nv_cvt_fp8_to_halfraw(sp[4 * lane + i], __NV_E4M3);
+                kv[i] = __half2float(__half(hr));
+            }
+        } else {
+            int c[4];
+            load_codes<KBITS>(sp, lane, c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kv[i] = s_cent[c[i]];
+            knorm = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_k_norm)));
+        }
+        float s[GM];
+#pragma unroll
+        for (int g = 0; g < GM; ++g)
+            s[g] = warp_sum(qv[g][0] * kv[0] + qv[g][1] * kv[1] + qv[g][2] * kv[2] + qv[g][3] * kv[3]) * knorm;
+
+        int vc[4];
+        load_codes<VBITS>(sp + a.g.off_v_data, lane, vc);
+        const float vs = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_scale)));
+        const float vz = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_zero)));
+        float vv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vv[i] = float(vc[i]) * vs + vz;
+
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            const float mn = fmaxf(m[g], s[g]);
+            const float al = expf(m[g] - mn), p = expf(s[g] - mn);
+            l[g] = l[g] * al + p;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[g][i] = acc[g][i] * al + p * vv[i];
+            m[g] = mn;
+        }
+    }
+
+    // merge the four warps' partials
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+        if (lane == 0) { s_m[warp][g] = m[g]; s_l[warp][g] = l[g]; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s_acc[warp][g][4 * lane + i] = acc[g][i];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
+        const int g = i / kHeadDim, d = i % kHeadDim;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][g]);
+        float lsum = 0.f, o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = s_m[w][g] == -INFINITY ? 0.f : expf(s_m[w][g] - M);
+            lsum += s_l[w][g] * f;
+            o += s_acc[w][g][d] * f;
+        }
+        float* mp = a.mid + (((long long)b * a.Hq + h * G + g) * S + split) * (kHeadDim + 1);
+        mp[d] = o / lsum;
+        if (d == 0) mp[kHeadDim] = M + logf(lsum);
+    }
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(kHeadDim) stage2_kernel(DecodeArgs a)
+{
+    const long long bh = blockIdx.x;   // b * Hq + hq
+    const int d = threadIdx.x, S = a.num_splits;
+    const float* mp = a.mid + bh * S * (kHeadDim + 1);
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, mp[s * (kHeadDim + 1) + kHeadDim]);
+    float W = 0.f, o = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < S; ++s) {
+            const float ls = mp[s * (kHeadDim + 1) + kHeadDim];
+            if (ls == -INFINITY) continue;
+            const float w = expf(ls - M);
+            W += w;
+            o += w * mp[s * (kHeadDim + 1) + d];
+        }
+        o /= W;
+    }
+    static_cast<TO*>(a.out)[bh * kHeadDim + d] = from_f32<TO>(o);
+    if (d == 0 && a.lse) a.lse[bh] = M == -INFINITY ? -INFINITY : M + logf(W);
+}
+
+template <typename TQ, bool FP8, int KB, int VB>
+cudaError_t launch_stage1_g(const DecodeArgs& a, cudaStream_t st)
+{
+    dim3 grid(a.num_splits, a.Hk, a.B);
+    if (a.G <= 1) stage1_kernel<TQ, FP8, KB, VB, 1><<<grid, kWarps * 32, 0, st>>>(a);
+    else if (a.G <= 2) stage1_kernel<TQ, FP8, KB, VB, 2><<<grid, kWarps * 32, 0, st>>>(a);
+    else if (a.G <= 4) stage1_kernel<TQ, FP8, KB, VB, 4><<<grid, kWarps * 32, 0, st>>>(a);
+    else if (a.G <= 8) stage1_kernel<TQ, FP8, KB, VB, 8><<<grid, kWarps * 32, 0, st>>>(a);
+    else stage1_kernel<TQ, FP8, KB, VB, 16><<<grid, kWarps * 32, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename TQ>
+cudaError_t launch_stage1(int preset, const DecodeArgs& a, cudaStream_t st)
+{
+    switch (preset) {
+    case TQ_K8V4:    return launch_stage1_g<TQ, true, 4, 4>(a, st);
+    case TQ_4BIT_NC: return launch_stage1_g<TQ, false, 4, 4>(a, st);
+    case TQ_K3V4_NC: return launch_stage1_g<TQ, false, 3, 4>(a, st);
+    case TQ_3BIT_NC: return launch_stage1_g<TQ, false, 3, 3>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,
+                                   int num_kv_heads, int block_size, int q_dtype, const void* query,
+                                   const uint8_t* kv_cache, long long num_blocks,
+                                   const int32_t* block_table, int block_table_stride,
+                                   const int32_t* seq_lens, int max_seq_len,
+                                   float softmax_scale, int num_splits,
+                                   const int8_t* signs, const float* centroids,
+                                   void* out, int out_dtype, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream)
+{
+    using namespace tq;
+    tq_layout L;
+    int rc = fill_layout(preset, head_dim, &L);
+    if (rc) return rc;
+    if (head_dim != kHeadDim || !block_size_ok(block_size) || !in_dtype_ok(q_dtype) ||
+        !out_dtype_ok(out_dtype))
+        return TQ_ERR_UNSUPPORTED;
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads ||
+        num_blocks < 0 || block_table_stride < 0 || max_seq_len < 0 || num_splits < 0 ||
+        num_splits > TQ_MAX_SPLITS)
+        return TQ_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > kMaxGroup) return TQ_ERR_UNSUPPORTED;
+    if (batch == 0) return TQ_OK;
+    if (!query || !kv_cache || !block_table || !seq_lens || !out || !workspace)
+        return TQ_ERR_INVALID_ARG;
+    if (!L.key_fp8 && (!signs || !centroids)) return TQ_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15) return TQ_ERR_INVALID_ARG;
+    const int S = num_splits ? num_splits : pick_splits(batch, num_kv_heads, max_seq_len);
+    if (workspace_bytes < tq_decode_workspace_bytes(batch, num_q_heads, S, head_dim))
+        return TQ_ERR_WORKSPACE;
+
+    DecodeArgs a;
+    a.query = query;
+    a.cache = kv_cache;
+    a.num_blocks = num_blocks;
+    a.block_table = block_table;
+    a.bt_stride = block_table_stride;
+    a.seq_lens = seq_lens;
+    a.scale = softmax_scale;
+    a.num_splits = S;
+    a.signs = signs;
+    a.centroids = centroids;
+    a.mid = static_cast<float*>(workspace);
+    a.out = out;
+    a.lse = lse;
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hk = num_kv_heads;
+    a.G = num_q_heads / num_kv_heads;
+    a.bs = block_size;
+    a.g = geom_of(L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    cudaError_t e = q_dtype == TQ_F16 ? launch_stage1<__half>(preset, a, st)
+                                      : launch_stage1<__nv_bfloat16>(preset, a, st);
+    if (e != cudaSuccess) return TQ_ERR_CUDA;
+    const unsigned grid2 = unsigned(batch) * num_q_heads;
+    if (out_dtype == TQ_F32) stage2_kernel<float><<<grid2, kHeadDim, 0, st>>>(a);
+    else if (out_dtype == TQ_F16) stage2_kernel<__half><<<grid2, kHeadDim, 0, st>>>(a);
+    else stage2_kernel<__nv_bfloat16><<<grid2, kHeadDim, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}

@@ -1,0 +1,236 @@
+// Fused quantising store of new K/V tokens into the combined paged cache.
+//
+// Method: "turboquant-plus.md" (Atlas TQ+), section "Background" (randomised
+// Hadamard rotation, Lloyd-Max codebook, matched-norm L2 scale, 3-bit packing
+// of 8 codes per 3 bytes); "vllm.v1.attention.backends.turboquant_attn" API
+// page, sections "_store_kv" and "do_kv_cache_update" (fused store of K and V
+// into one slot per (block, token, kv head)).
+//
+// Mapping: one CTA per token (grid-stride), one warp per kv head, 4 consecutive
+// coordinates per lane.  The rotation is a warp-shuffle Walsh-Hadamard
+// transform in registers; the bucketize is a branch-free binary search over
+// midpoints in shared memory; each warp assembles its slot in shared memory
+// and the CTA writes the token's Hk contiguous slots with 16-byte stores.
+// The value path uses explicitly rounded fp32 operations so the stored bytes
+// are reproducible bit for bit.
+#include "tq.h"
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+struct StoreArgs {
+    const void* key;
+    const void* value;
+    long long key_stride, value_stride;   // elements between tokens
+    const int64_t* slot_mapping;
+    uint8_t* cache;
+    long long num_slots;                  // num_blocks * block_size
+    const int8_t* signs;
+    const float* centroids;
+    const float* midpoints;
+    int num_tokens, num_kv_heads;
+    int slot_size;                        // unpadded
+    SlotGeom g;
+};
+
+// Pack the 4 codes of every lane (code 4*lane+i = c[i]) as a BITS-wide
+// LSB-first bitstream starting at dst.  All lanes of the warp take part.
+template <int BITS>
+__device__ __forceinline__ void pack_codes(uint8_t* dst, const int (&c)[4], int lane)
+{
+    const uint32_t w = uint32_t(c[0]) | uint32_t(c[1]) << BITS | uint32_t(c[2]) << (2 * BITS) |
+                       uint32_t(c[3]) << (3 * BITS);
+    if constexpr (BITS == 4) {
+        dst[2 * lane] = uint8_t(w);
+        dst[2 * lane + 1] = uint8_t(w >> 8);
+    } else if constexpr (BITS == 2) {
+        dst[lane] = uint8_t(w);
+    } else {  // 3 bits: lane pairs form 24 bits = 3 bytes
+        static_assert(BITS == 3, "2, 3 or 4 bits");
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, w, 1);
+        if (!(lane & 1)) {
+            const uint32_t x = w | (hi << 12);
+            uint8_t* p = dst + 3 * (lane >> 1);
+            p[0] = uint8_t(x);
+            p[1] = uint8_t(x >> 8);
+            p[2] = uint8_t(x >> 16);
+        }
+    }
+}
+
+__device__ __forceinline__ void put_u16(uint8_t* p, uint16_t v)
+{
+    p[0] = uint8_t(v);
+    p[1] = uint8_t(v >> 8);
+}
+
+template <typename T, bool KEY_FP8, int KBITS, int VBITS, bool NORM_CORR>
+__global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float s_cent[16], s_mid[16];
+    const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
+    const int S = a.g.slot;
+    const int row_bytes = a.num_kv_heads * S;
+
+    if constexpr (!KEY_FP8) {
+        constexpr int NC = 1 << KBITS;
+        if (threadIdx.x < NC) s_cent[threadIdx.x] = a.centroids[threadIdx.x];
+        if (threadIdx.x < NC - 1) s_mid[threadIdx.x] = a.midpoints[threadIdx.x];
+    }
+    float sgn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sgn[i] = float(a.signs[4 * lane + i]);
+    __syncthreads();
+
+    const T* K = static_cast<const T*>(a.key);
+    const T* V = static_cast<const T*>(a.value);
+
+    for (int n = blockIdx.x; n < a.num_tokens; n += gridDim.x) {
+        const long long slot_idx = a.slot_mapping[n];
+        if (slot_idx < 0 || slot_idx >= a.num_slots) continue;   // uniform across the CTA
+        uint8_t* row = smem;
+        uint8_t* dst = row + h * S;
+
+        float k[4], v[4];
+        const T* kp = K + n * a.key_stride + (long long)h * kHeadDim + 4 * lane;
+        const T* vp = V + n * a.value_stride + (long long)h * kHeadDim + 4 * lane;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { k[i] = to_f32(kp[i]); v[i] = to_f32(vp[i]); }
+
+        // ---------------- keys
+        if constexpr (KEY_FP8) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[4 * lane + i] = __nv_cvt_float_to_fp8(k[i], __NV_SATFINITE, __NV_E4M3);
+        } else {
+            const float n2 = warp_sum(k[0] * k[0] + k[1] * k[1] + k[2] * k[2] + k[3] * k[3]);
+            const float nrm = __fsqrt_rn(n2);
+            float x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i] = sgn[i] * k[i];
+            fwht128_warp(x, lane);
+            // y = H(s.k)/||k|| with H = Sylvester / sqrt(128)
+            const float inv = nrm > 0.f ? __fdiv_rn(0.08838834764831845f, nrm) : 0.f;
+            int idx[4];
+            float cn = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float y = x[i] * inv;
+                int j = 0;
+#pragma unroll
+                for (int step = 1 << (KBITS - 1); step; step >>= 1)
+                    if (y > s_mid[j + step - 1]) j += step;
+                idx[i] = j;
+                const float c = s_cent[j];
+                cn += c * c;
+            }
+            cn = warp_sum(cn);
+            const float stored = NORM_CORR ? __fdiv_rn(nrm, __fsqrt_rn(cn)) : nrm;
+            pack_codes<KBITS>(dst, idx, lane);
+            if (lane == 0) put_u16(dst + a.g.off_k_norm, __half_as_ushort(__float2half_rn(stored)));
+        }
+
+        // ---------------- values: asymmetric min/max uniform codes
+        {
+            constexpr int QMAX = (1 << VBITS) - 1;
+            const float lo = warp_min(fminf(fminf(v[0], v[1]), fminf(v[2], v[3])));
+            const float hi = warp_max(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+            const __half scale16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), float(QMAX)));
+            const __half zero16 = __float2half_rn(lo);
+            const float sc = __half2float(scale16), z = __half2float(zero16);
+            int code[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float r = 0.f;
+                if (sc > 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[i], z), sc)), 0.f), float(QMAX));
+                code[i] = int(r);
+            }
+            pack_codes<VBITS>(dst + a.g.off_v_data, code, lane);
+            if (lane == 0) {
+                put_u16(dst + a.g.off_v_scale, __half_as_ushort(scale16));
+                put_u16(dst + a.g.off_v_zero, __half_as_ushort(zero16));
+                if (a.slot_size < S) dst[S - 1] = 0;
+            }
+        }
+        __syncthreads();
+
+        // ---------------- write the token's Hk contiguous slots
+        uint8_t* out = a.cache + slot_idx * (long long)row_bytes;
+        if ((row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+            const uint4* src4 = reinterpret_cast<const uint4*>(row);
+            uint4* dst4 = reinterpret_cast<uint4*>(out);
+            for (int i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) dst4[i] = src4[i];
+        } else {
+            const uint16_t* src2 = reinterpret_cast<const uint16_t*>(row);
+            uint16_t* dst2 = reinterpret_cast<uint16_t*>(out);
+            for (int i = threadIdx.x; i < row_bytes / 2; i += blockDim.x) dst2[i] = src2[i];
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+cudaError_t launch_store_t(int preset, const StoreArgs& a, cudaStream_t st)
+{
+    const int threads = 32 * a.num_kv_heads;
+    const size_t smem = size_t(a.num_kv_heads) * a.g.slot;
+    int grid = a.num_tokens < kNumSMs * 8 ? a.num_tokens : kNumSMs * 8;
+    switch (preset) {
+    case TQ_K8V4:    store_kernel<T, true, 4, 4, false><<<grid, threads, smem, st>>>(a); break;
+    case TQ_4BIT_NC: store_kernel<T, false, 4, 4, true><<<grid, threads, smem, st>>>(a); break;
+    case TQ_K3V4_NC: store_kernel<T, false, 3, 4, true><<<grid, threads, smem, st>>>(a); break;
+    case TQ_3BIT_NC: store_kernel<T, false, 3, 3, true><<<grid, threads, smem, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int tq_store(int preset, int head_dim, int num_tokens, int num_kv_heads, int block_size,
+                        int in_dtype, const void* key, const void* value,
+                        long long key_stride_tok, long long value_stride_tok,
+                        const int64_t* slot_mapping, uint8_t* kv_cache, long long num_blocks,
+                        const int8_t* signs, const float* centroids, const float* midpoints,
+                        void* stream)
+{
+    using namespace tq;
+    tq_layout L;
+    int rc = fill_layout(preset, head_dim, &L);
+    if (rc) return rc;
+    if (head_dim != kHeadDim || !block_size_ok(block_size) || !in_dtype_ok(in_dtype))
+        return TQ_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_kv_heads < 1 || num_kv_heads > 32 || num_blocks < 0)
+        return TQ_ERR_INVALID_ARG;
+    if (num_tokens == 0) return TQ_OK;
+    if (!key || !value || !slot_mapping || !kv_cache || !signs) return TQ_ERR_INVALID_ARG;
+    if (!L.key_fp8 && (!centroids || !midpoints)) return TQ_ERR_INVALID_ARG;
+    if (key_stride_tok < (long long)num_kv_heads * head_dim ||
+        value_stride_tok < (long long)num_kv_heads * head_dim)
+        return TQ_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(kv_cache) & 15) return TQ_ERR_INVALID_ARG;
+
+    StoreArgs a;
+    a.key = key;
+    a.value = value;
+    a.key_stride = key_stride_tok;
+    a.value_stride = value_stride_tok;
+    a.slot_mapping = slot_mapping;
+    a.cache = kv_cache;
+    a.num_slots = num_blocks * (long long)block_size;
+    a.signs = signs;
+    a.centroids = centroids;
+    a.midpoints = midpoints;
+    a.num_tokens = num_tokens;
+    a.num_kv_heads = num_kv_heads;
+    a.slot_size = L.slot_size;
+    a.g = geom_of(L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = in_dtype == TQ_F16 ? launch_store_t<__half>(preset, a, st)
+                                       : launch_store_t<__nv_bfloat16>(preset, a, st);
+    return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}

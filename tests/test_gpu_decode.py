@@ -1,0 +1,135 @@
+"""GPU parity of split-K decode attention (through the C ABI) against the
+oracle's dense attention over the oracle's cache, and end to end (GPU store
++ GPU decode against oracle store + oracle decode)."""
+import numpy as np
+import pytest
+import torch
+
+import quantized_kv_cache_04_gb300 as tq
+from _helpers import check_decode, codebook, paged_problem, to_f32
+
+pytestmark = pytest.mark.gpu
+PRESETS = [0, 1, 2, 3]
+
+
+def _gpu_decode(preset, q, cache_np, bt, seq_lens, Hk, bs, signs, c32, num_splits=0,
+                out_dtype=torch.float32, cache_dev=None):
+    dev = torch.device("cuda")
+    B, Hq, D = q.shape
+    cache = cache_dev if cache_dev is not None else torch.from_numpy(cache_np).to(dev)
+    btd = torch.from_numpy(np.ascontiguousarray(bt)).to(dev)
+    sl = torch.from_numpy(np.asarray(seq_lens, np.int32)).to(dev)
+    L = tq.tq_get_layout(preset)
+    sg = torch.from_numpy(signs).to(dev)
+    cc = torch.from_numpy(c32).to(dev) if not L["key_fp8"] else None
+    maxlen = int(max(seq_lens)) if len(seq_lens) else 0
+    S = num_splits or tq.tq_decode_pick_splits(B, Hq, Hk, maxlen)
+    ws = torch.empty(max(16, tq.tq_decode_workspace_bytes(B, Hq, S, D)), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((B, Hq, D), dtype=out_dtype, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    tq.decode_attention(preset, q.to(dev).contiguous(), cache, btd, sl, maxlen, Hk, bs, sg, cc,
+                        out, lse, ws, num_splits=num_splits)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+CASES = [  # (G, Hk, bs, seq_lens, splits)
+    (4, 2, 16, [512], 0),
+    (8, 2, 64, [1000, 1, 0, 130], 7),
+    (1, 4, 32, [65, 300], 1),
+    (16, 1, 128, [1500], 64),
+    (6, 2, 16, [33, 200], 3),
+    (4, 8, 32, [17, 0, 256, 97, 5], 0),
+]
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("qdtype", [torch.float16, torch.bfloat16])
+def test_decode_on_oracle_cache(orc, preset, case, qdtype):
+    G, Hk, bs, seq_lens, S = CASES[case]
+    rng = np.random.default_rng(1000 * preset + 10 * case + (qdtype == torch.bfloat16))
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng,
+                       dtype="bfloat16" if qdtype == torch.bfloat16 else "float16")
+    B = len(seq_lens)
+    q = torch.from_numpy(rng.normal(size=(B, G * Hk, 128)) * 1.5).to(qdtype)
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], pb["bt"],
+                                    np.asarray(seq_lens, np.int32), Hk, bs, pb["signs"],
+                                    pb["c32"])
+    o, l = _gpu_decode(preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"],
+                       pb["c32"], S)
+    check_decode(o, l, ref_o, ref_l, f"preset {preset} case {case}")
+    # output in the query dtype: within one ulp of the exact result rounded once
+    o16, _ = _gpu_decode(preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"],
+                         pb["c32"], S, out_dtype=qdtype)
+    ref16 = torch.from_numpy(ref_o).to(qdtype).float().numpy()
+    eps = 2.0 ** -10 if qdtype == torch.float16 else 2.0 ** -7
+    ulp = eps * np.maximum(2.0 ** np.floor(np.log2(np.maximum(np.abs(ref16), 2.0 ** -14))),
+                           2.0 ** -14)
+    assert np.all(np.abs(o16 - ref16) <= ulp * 1.0001)
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_split_count_invariance(orc, preset):
+    """Results do not depend on the split count beyond rounding."""
+    rng = np.random.default_rng(77 + preset)
+    seq_lens, Hk, bs = [3000, 45], 2, 32
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng)
+    q = torch.from_numpy(rng.normal(size=(2, 8, 128))).to(torch.float16)
+    base = _gpu_decode(preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"], pb["c32"], 1)
+    for S in (2, 5, 64, 256):
+        o, l = _gpu_decode(preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"],
+                           pb["c32"], S)
+        assert np.max(np.abs(o - base[0])) < 1e-4
+        assert np.max(np.abs(l - base[1])) < 1e-5
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_end_to_end_store_then_decode(orc, preset):
+    """GPU store + GPU decode against oracle store + oracle decode."""
+    rng = np.random.default_rng(500 + preset)
+    seq_lens, Hk, G, bs = [700, 33, 1], 4, 4, 16
+    dev = torch.device("cuda")
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng)   # oracle cache + inputs
+    L = tq.tq_get_layout(preset)
+    cache = torch.zeros(pb["cache"].shape, dtype=torch.uint8, device=dev)
+    cache[pb["guard"]] = 0xFF
+    sg = torch.from_numpy(pb["signs"]).to(dev)
+    cc = torch.from_numpy(pb["c32"]).to(dev) if not L["key_fp8"] else None
+    mm = torch.from_numpy(pb["m32"]).to(dev) if not L["key_fp8"] else None
+    for b, n in enumerate(seq_lens):
+        t = np.arange(n)
+        sm = torch.from_numpy(pb["bt"][b, t // bs].astype(np.int64) * bs + t % bs).to(dev)
+        tq.store(preset, pb["K"][b].to(dev), pb["V"][b].to(dev), sm, cache, bs, sg, cc, mm)
+    q = torch.from_numpy(rng.normal(size=(len(seq_lens), G * Hk, 128))).to(torch.float16)
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], pb["bt"],
+                                    np.asarray(seq_lens, np.int32), Hk, bs, pb["signs"], pb["c32"])
+    o, l = _gpu_decode(preset, q, None, pb["bt"], seq_lens, Hk, bs, pb["signs"], pb["c32"],
+                       cache_dev=cache)
+    check_decode(o, l, ref_o, ref_l, f"e2e preset {preset}")
+
+
+def test_planted_key_peaked_softmax(orc):
+    """A key aligned with the query (logit ~ 12) dominates each split: the
+    LSE merge of peaked partials stays within 1e-4."""
+    rng = np.random.default_rng(4)
+    preset, Hk, G, bs, n = 3, 2, 4, 128, 8192
+    pb = paged_problem(orc, preset, [n], Hk, bs, rng, dtype="bfloat16")
+    q = torch.from_numpy(rng.normal(size=(1, G * Hk, 128)) * 1.2).to(torch.bfloat16)
+    # plant keys aligned with head-0 queries every 1024 tokens, re-store with the oracle
+    K = pb["K"][0].clone()
+    for t in range(512, n, 1024):
+        for h in range(Hk):
+            d = to_f32(q[0, h * G]).astype(np.float64)
+            K[t, h] = torch.from_numpy(1.1 * np.sqrt(128) * d / np.linalg.norm(d)).to(torch.bfloat16)
+    tt = np.arange(n)
+    sm = pb["bt"][0, tt // bs].astype(np.int64) * bs + tt % bs
+    orc.store(preset, to_f32(K), to_f32(pb["V"][0]), sm, pb["cache"], bs, pb["signs"],
+              pb["c32"], pb["m32"])
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], pb["bt"],
+                                    np.array([n], np.int32), Hk, bs, pb["signs"], pb["c32"])
+    assert ref_l.max() > 8
+    for S in (1, 8, 64):
+        o, l = _gpu_decode(preset, q, pb["cache"], pb["bt"], [n], Hk, bs, pb["signs"], pb["c32"], S)
+        check_decode(o, l, ref_o, ref_l, f"planted S={S}")
