@@ -36,34 +36,34 @@ struct StoreArgs {
 };
 
 // Pack the 4 codes of every lane (code 4*lane+i = c[i]) as a BITS-wide
-// LSB-first bitstream starting at dst.  All lanes of the warp take part.
+// LSB-first bitstream starting at dst (2-byte aligned).  All lanes of the warp
+// take part.  Every shared-memory write is an aligned 16-bit store.
 template <int BITS>
 __device__ __forceinline__ void pack_codes(uint8_t* dst, const int (&c)[4], int lane)
 {
     const uint32_t w = uint32_t(c[0]) | uint32_t(c[1]) << BITS | uint32_t(c[2]) << (2 * BITS) |
                        uint32_t(c[3]) << (3 * BITS);
+    uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
     if constexpr (BITS == 4) {
-        dst[2 * lane] = uint8_t(w);
-        dst[2 * lane + 1] = uint8_t(w >> 8);
-    } else if constexpr (BITS == 2) {
-        dst[lane] = uint8_t(w);
-    } else {  // 3 bits: lane pairs form 24 bits = 3 bytes
-        static_assert(BITS == 3, "2, 3 or 4 bits");
+        d16[lane] = uint16_t(w);
+    } else if constexpr (BITS == 2) {   // lane pairs form 16 bits
         const uint32_t hi = __shfl_down_sync(0xffffffffu, w, 1);
-        if (!(lane & 1)) {
-            const uint32_t x = w | (hi << 12);
-            uint8_t* p = dst + 3 * (lane >> 1);
-            p[0] = uint8_t(x);
-            p[1] = uint8_t(x >> 8);
-            p[2] = uint8_t(x >> 16);
-        }
+        if (!(lane & 1)) d16[lane >> 1] = uint16_t(w | (hi << 8));
+    } else {                            // 3 bits: groups of 4 lanes form 48 bits = 3 words
+        static_assert(BITS == 3, "2, 3 or 4 bits");
+        const int g = lane & ~3, r = lane & 3;
+        const uint64_t w0 = __shfl_sync(0xffffffffu, w, g);
+        const uint64_t w1 = __shfl_sync(0xffffffffu, w, g + 1);
+        const uint64_t w2 = __shfl_sync(0xffffffffu, w, g + 2);
+        const uint64_t w3 = __shfl_sync(0xffffffffu, w, g + 3);
+        const uint64_t bits = w0 | (w1 << 12) | (w2 << 24) | (w3 << 36);
+        if (r < 3) d16[3 * (g >> 2) + r] = uint16_t(bits >> (16 * r));
     }
 }
 
 __device__ __forceinline__ void put_u16(uint8_t* p, uint16_t v)
 {
-    p[0] = uint8_t(v);
-    p[1] = uint8_t(v >> 8);
+    *reinterpret_cast<uint16_t*>(p) = v;   // p is 2-byte aligned: slots and fields are even
 }
 
 template <typename T, bool KEY_FP8, int KBITS, int VBITS, bool NORM_CORR>
@@ -102,9 +102,12 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
 
         // ---------------- keys
         if constexpr (KEY_FP8) {
+            uint32_t b[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                dst[4 * lane + i] = __nv_cvt_float_to_fp8(k[i], __NV_SATFINITE, __NV_E4M3);
+            for (int i = 0; i < 4; ++i) b[i] = __nv_cvt_float_to_fp8(k[i], __NV_SATFINITE, __NV_E4M3);
+            uint16_t* d16 = reinterpret_cast<uint16_t*>(dst + 4 * lane);
+            d16[0] = uint16_t(b[0] | (b[1] << 8));
+            d16[1] = uint16_t(b[2] | (b[3] << 8));
         } else {
             const float n2 = warp_sum(k[0] * k[0] + k[1] * k[1] + k[2] * k[2] + k[3] * k[3]);
             const float nrm = __fsqrt_rn(n2);

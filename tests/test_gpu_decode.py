@@ -61,13 +61,14 @@ def test_decode_on_oracle_cache(orc, preset, case, qdtype):
                        pb["c32"], S)
     check_decode(o, l, ref_o, ref_l, f"preset {preset} case {case}")
     # output in the query dtype: within one ulp of the exact result rounded once
+    # (plus the fp32 path's own error, far below the 2e-3 bar, for tiny values)
     o16, _ = _gpu_decode(preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"],
                          pb["c32"], S, out_dtype=qdtype)
     ref16 = torch.from_numpy(ref_o).to(qdtype).float().numpy()
     eps = 2.0 ** -10 if qdtype == torch.float16 else 2.0 ** -7
     ulp = eps * np.maximum(2.0 ** np.floor(np.log2(np.maximum(np.abs(ref16), 2.0 ** -14))),
                            2.0 ** -14)
-    assert np.all(np.abs(o16 - ref16) <= ulp * 1.0001)
+    assert np.all(np.abs(o16 - ref16) <= ulp * 1.0001 + 2e-5)
 
 
 @pytest.mark.parametrize("preset", PRESETS)

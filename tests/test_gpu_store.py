@@ -37,7 +37,7 @@ def _run_store(orc, preset, K, V, slot_mapping, num_blocks, bs, key_view=None, v
     return cache.cpu().numpy(), s, c32, m32
 
 
-def _check(orc, preset, K, V, slot_mapping, cache, s, c32, m32, bs):
+def _check(orc, preset, K, V, slot_mapping, cache, s, c32, m32, bs, bound_fraction=True):
     N, Hk, D = K.shape
     flat = cache.reshape(-1, Hk, cache.shape[-1])
     live = slot_mapping >= 0
@@ -45,7 +45,8 @@ def _check(orc, preset, K, V, slot_mapping, cache, s, c32, m32, bs):
     kf = to_f32(K)[live].reshape(-1, D)
     vf = to_f32(V)[live].reshape(-1, D)
     flips, codes = compare_store(orc, preset, rows, kf, vf, s, c32, m32)
-    assert flips <= max(1, math.ceil(TIE_FRACTION * codes)), (flips, codes)
+    if bound_fraction:
+        assert flips <= max(1, math.ceil(TIE_FRACTION * codes)), (flips, codes)
     untouched = np.setdiff1d(np.arange(flat.shape[0]), slot_mapping[live])
     assert np.all(flat[untouched] == SENTINEL)
     return flips, codes
@@ -72,7 +73,11 @@ def test_store_parity(orc, preset, dtype, Hk, N, bs):
 @pytest.mark.parametrize("preset", PRESETS)
 def test_store_edge_values(orc, preset):
     """Zero and constant vectors, tiny and large magnitudes (fp8 saturation),
-    one-hot keys, and a strided (non-contiguous token stride) input view."""
+    one-hot keys, and a strided (non-contiguous token stride) input view.
+    Structured keys put many rotated coordinates exactly on a decision
+    boundary (e.g. Hadamard cancellation to 0 against the middle midpoint),
+    so every flip must still be an adjacent code at a tie, but the 1e-4
+    fraction (a bar for random data) is not applied here."""
     Hk, D, bs = 4, 128, 16
     rows = [np.zeros(D), np.full(D, 3.0), np.full(D, -1e-6), np.eye(D)[7] * 5,
             np.linspace(-600, 600, D), np.linspace(-1, 1, D) * 1e-4,
@@ -91,7 +96,7 @@ def test_store_edge_values(orc, preset):
         sm = np.arange(N, dtype=np.int64) * 3 + 1
         cache, s, c32, m32 = _run_store(orc, preset, K, V, sm, (3 * N) // bs + 2, bs,
                                         key_view=kview, value_view=vview)
-        _check(orc, preset, K, V, sm, cache, s, c32, m32, bs)
+        _check(orc, preset, K, V, sm, cache, s, c32, m32, bs, bound_fraction=False)
 
 
 def test_store_padding_only_and_large_batch(orc):
