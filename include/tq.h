@@ -14,9 +14,12 @@
  * Slot interior (byte offsets in tq_layout):
  *   [key data][k_norm fp16, MSE presets only][value data][v_scale fp16][v_zero fp16][pad to even]
  * key data is either D bytes of FP8 E4M3 (k8v4) or a b_k-bit packed code
- * stream; value data is a b_v-bit packed code stream.  Codes are packed
- * LSB-first: code i occupies bits [b*i, b*i+b) of the little-endian byte
- * stream.  Sizes per "vllm.v1.attention.backends.turboquant_attn" API page,
+ * stream; value data is a b_v-bit packed code stream.  4-bit codes: two per
+ * byte, low nibble first.  3-bit codes (8 per 3 bytes): groups of 32 codes
+ * in 12 bytes read as little-endian 32-bit words W0, W1, W2; code 8w+i
+ * (i < 8, w < 3) sits in bits [4i, 4i+3) of Ww and bit w of code 24+i in bit
+ * 4i+3 of Ww, so every code starts on a nibble boundary.  Sizes per
+ * "vllm.v1.attention.backends.turboquant_attn" API page,
  * section "__init__" (mse bytes, value data bytes) and section
  * "_continuation_prefill" (field order k_norm, v_scale, v_zero).
  *
@@ -151,7 +154,9 @@ size_t tq_decode_workspace_bytes(int batch, int num_q_heads, int num_splits, int
  *     block_table[b*block_table_stride + t/block_size]; score = softmax_scale *
  *     k_norm * <q_rot, c[idx]> (MSE) or softmax_scale * <q, k_fp8> (k8v4);
  *     online softmax; v_hat = code * v_scale + v_zero accumulated.
- *     Split s covers [s*c, min(L, (s+1)*c)), c = ceil(L / num_splits).
+ *     Splits are consecutive token ranges (the tensor-core kernel rounds
+ *     their length up to whole 16-token tiles); the result does not depend
+ *     on the split count beyond rounding.
  *   stage 2: o = sum_s w_s o_s / sum_s w_s, w_s = exp(lse_s - max lse),
  *     lse = max + ln sum w_s (natural log, scale included).
  * seq_lens[b] == 0 gives o = 0 and lse = -inf.
@@ -174,6 +179,13 @@ int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,
                         const int8_t* signs, const float* centroids,
                         void* out, int out_dtype, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Which stage-1 kernel tq_decode_attention runs for this shape (host only):
+ * 1 = tensor-core stage 1 (FP8 or 3-bit keys, 3/4-bit values, group size
+ * <= 8, num_kv_heads <= 16, token row = num_kv_heads * slot a multiple of 16
+ * bytes and at most ~1.7 KB);
+ * 0 = CUDA-core stage 1 (every other supported shape); -1 = unsupported. */
+int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, int num_kv_heads);
 
 /* Human-readable text of a status code (static storage). */
 const char* tq_status_string(int status);

@@ -260,10 +260,26 @@ static const double* orc_hadamard_cached(int D)
 
 /* ======================================================================
  * Bit packing.  [Atlas] "Background": 3-bit data is 8 values per 3 bytes;
- * 4-bit is two per byte, 2-bit four per byte.  Bit order is not given on
- * the pages: LSB-first, code i occupies bits [b*i, b*i + b) of the
- * little-endian byte stream.
+ * 4-bit is two per byte, 2-bit four per byte.  The bit order is not on the
+ * pages.  Readings used here:
+ *  - 2, 4 and 8 bits: LSB-first, code i occupies bits [b*i, b*i + b) of the
+ *    little-endian byte stream (4-bit: low nibble first).
+ *  - 3 bits: groups of 32 codes in 12 bytes, read as three little-endian
+ *    32-bit words W0, W1, W2.  For i = 0..7 and w = 0..2, bits [4i, 4i+3) of
+ *    Ww hold code 8w + i, and bit 4i+3 of Ww holds bit w of code 24 + i.
+ *    (Same density, 8 codes per 3 bytes; every code's low bits sit at a
+ *    nibble boundary.)  n must be a multiple of 32.
  * ==================================================================== */
+static void orc_setbit(uint8_t* out, int bit) { out[bit / 8] |= (uint8_t)(1u << (bit % 8)); }
+static int orc_getbit(const uint8_t* in, int bit) { return (in[bit / 8] >> (bit % 8)) & 1; }
+
+/* bit position (within the group's 96 bits) of bit j of code i, 3-bit layout */
+static int orc_bitpos3(int i, int j)
+{
+    if (i < 24) return 32 * (i / 8) + 4 * (i % 8) + j;
+    return 32 * j + 4 * (i - 24) + 3;
+}
+
 void orc_pack(const int* codes, int n, int bits, uint8_t* out)
 {
     int nbytes = (n * bits + 7) / 8;
@@ -271,8 +287,8 @@ void orc_pack(const int* codes, int n, int bits, uint8_t* out)
     for (int i = 0; i < n; ++i)
         for (int j = 0; j < bits; ++j)
             if ((codes[i] >> j) & 1) {
-                int bit = i * bits + j;
-                out[bit / 8] |= (uint8_t)(1u << (bit % 8));
+                if (bits == 3) orc_setbit(out, 96 * (i / 32) + orc_bitpos3(i % 32, j));
+                else           orc_setbit(out, i * bits + j);
             }
 }
 
@@ -281,8 +297,8 @@ void orc_unpack(const uint8_t* in, int n, int bits, int* codes)
     for (int i = 0; i < n; ++i) {
         int c = 0;
         for (int j = 0; j < bits; ++j) {
-            int bit = i * bits + j;
-            c |= ((in[bit / 8] >> (bit % 8)) & 1) << j;
+            int bit = bits == 3 ? 96 * (i / 32) + orc_bitpos3(i % 32, j) : i * bits + j;
+            c |= orc_getbit(in, bit) << j;
         }
         codes[i] = c;
     }

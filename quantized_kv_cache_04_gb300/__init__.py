@@ -9,12 +9,12 @@ from __future__ import annotations
 from . import _lib
 from ._lib import (PRESETS, TQ_3BIT_NC, TQ_4BIT_NC, TQ_BF16, TQ_F16, TQ_F32, TQ_K3V4_NC,
                    TQ_K8V4, TQError, decode_attention, load, store, tq_build_codebook,
-                   tq_decode_attention, tq_decode_pick_splits, tq_decode_workspace_bytes,
+                   tq_decode_attention, tq_decode_kernel_kind, tq_decode_pick_splits, tq_decode_workspace_bytes,
                    tq_get_layout, tq_make_signs, tq_status_string, tq_store, tq_version)
 
 __all__ = ["PRESETS", "TQ_K8V4", "TQ_4BIT_NC", "TQ_K3V4_NC", "TQ_3BIT_NC", "TQ_F16", "TQ_BF16",
            "TQ_F32", "TQError", "TQCache", "load", "store", "decode_attention", "tq_store",
-           "tq_decode_attention", "tq_get_layout", "tq_build_codebook", "tq_make_signs",
+           "tq_decode_attention", "tq_decode_kernel_kind", "tq_get_layout", "tq_build_codebook", "tq_make_signs",
            "tq_decode_workspace_bytes", "tq_decode_pick_splits", "tq_status_string", "tq_version"]
 
 SIGN_SEED = 42          # per-layer seed = 42 + 1337 * layer

@@ -70,6 +70,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                       _c_int, ctypes.c_float, _c_int, _c_vp,
                                                       _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_sz,
                                                       _c_vp])
+    L.tq_decode_kernel_kind.argtypes = [_c_int] * 4
     L.tq_status_string.argtypes = [_c_int]
     L.tq_status_string.restype = ctypes.c_char_p
     L.tq_version.restype = _c_int
@@ -117,6 +118,12 @@ def tq_make_signs(head_dim: int, seed: int = 42):
 def tq_decode_pick_splits(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int) -> int:
     return load().tq_decode_pick_splits(int(batch), int(num_q_heads), int(num_kv_heads),
                                         int(max_seq_len))
+
+
+def tq_decode_kernel_kind(preset: int, head_dim: int, num_q_heads: int, num_kv_heads: int) -> int:
+    """1 = tensor-core stage 1, 0 = CUDA-core stage 1, -1 = unsupported shape."""
+    return load().tq_decode_kernel_kind(int(preset), int(head_dim), int(num_q_heads),
+                                        int(num_kv_heads))
 
 
 def tq_decode_workspace_bytes(batch: int, num_q_heads: int, num_splits: int, head_dim: int = 128) -> int:

@@ -7,7 +7,9 @@
 // shared mid_o / lse scratch); "turboquant-plus.md", "weight pre-rotation"
 // note (<Q H, H K> = <Q, K>, so q is rotated once and keys stay rotated).
 //
-// This file holds the CUDA-core path: one CTA per (split, kv head, sequence),
+// This file holds the host entry point, stage 2 (the log-sum-exp merge) and
+// the CUDA-core stage 1 used for shapes the tensor-core stage 1
+// (tq_decode_mma.cu) does not serve: one CTA per (split, kv head, sequence),
 // four warps striding over the split's tokens, 4 coordinates per lane, fp32
 // scores and online softmax, partials merged across warps in shared memory.
 #include "tq.h"
@@ -21,9 +23,9 @@ namespace tq {
 int pick_splits(int batch, int num_kv_heads, int max_seq_len)
 {
     if (batch <= 0 || num_kv_heads <= 0 || max_seq_len <= 0) return 1;
-    const long long units = (long long)batch * num_kv_heads;
-    long long s = (4LL * kNumSMs + units - 1) / units;           // ~4 CTAs per SM
-    const long long by_len = (max_seq_len + 255) / 256;          // >= 256 tokens per split
+    // about four CTAs of (split, sequence) per SM, each split >= 256 tokens
+    long long s = (4LL * kNumSMs + batch - 1) / batch;
+    const long long by_len = (max_seq_len + 255) / 256;
     if (s > by_len) s = by_len;
     if (s < 1) s = 1;
     if (s > TQ_MAX_SPLITS) s = TQ_MAX_SPLITS;
@@ -52,21 +54,34 @@ struct DecodeArgs {
 
 constexpr int kWarps = 4;
 
-// Codes 4*lane .. 4*lane+3 of a BITS-wide LSB-first stream starting at p.
+// Codes 4*lane .. 4*lane+3 of a packed code stream starting at p (2-byte
+// aligned).  4 bits: low nibble first.  3 bits: 32-code groups of three
+// 32-bit words W0..W2, code 8w+i in bits [4i, 4i+3) of Ww, bit w of code
+// 24+i in bit 4i+3 of Ww.
 template <int BITS>
 __device__ __forceinline__ void load_codes(const uint8_t* p, int lane, int (&c)[4])
 {
-    uint32_t w;
     if constexpr (BITS == 4) {
-        w = ld_u16(p + 2 * lane);
+        const uint32_t w = ld_u16(p + 2 * lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = (w >> (4 * i)) & 15u;
     } else {
         static_assert(BITS == 3, "3 or 4 bits");
-        const int bit = 12 * lane;
-        const uint8_t* q = p + (bit >> 3);
-        w = (uint32_t(q[0]) | uint32_t(q[1]) << 8) >> (bit & 7);
-    }
+        const int j = lane & 7;
+        const uint8_t* g = p + 12 * (lane >> 3);
+        if (j < 6) {
+            const uint32_t w = ld_u16(g + 4 * (j >> 1) + 2 * (j & 1));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = (w >> (BITS * i)) & ((1u << BITS) - 1);
+            for (int i = 0; i < 4; ++i) c[i] = (w >> (4 * i)) & 7u;
+        } else {
+            const int h = j - 6;
+            const uint32_t w0 = ld_u16(g + 2 * h), w1 = ld_u16(g + 4 + 2 * h), w2 = ld_u16(g + 8 + 2 * h);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                c[i] = ((w0 >> (4 * i + 3)) & 1u) | (((w1 >> (4 * i + 3)) & 1u) << 1) |
+                       (((w2 >> (4 * i + 3)) & 1u) << 2);
+        }
+    }
 }
 
 template <typename TQ, bool KEY_FP8, int KBITS, int VBITS, int GM>
@@ -305,12 +320,29 @@ extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_
     a.g = geom_of(L);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    cudaError_t e = q_dtype == TQ_F16 ? launch_stage1<__half>(preset, a, st)
-                                      : launch_stage1<__nv_bfloat16>(preset, a, st);
-    if (e != cudaSuccess) return TQ_ERR_CUDA;
+    if (mma_stage1_supported(L, num_kv_heads, a.G)) {
+        rc = launch_mma_stage1(L, q_dtype, query, kv_cache, block_table, block_table_stride, seq_lens,
+                               softmax_scale, S, signs, centroids, a.mid, batch, num_q_heads,
+                               num_kv_heads, block_size, st);
+        if (rc) return rc;
+    } else {
+        cudaError_t e = q_dtype == TQ_F16 ? launch_stage1<__half>(preset, a, st)
+                                          : launch_stage1<__nv_bfloat16>(preset, a, st);
+        if (e != cudaSuccess) return TQ_ERR_CUDA;
+    }
     const unsigned grid2 = unsigned(batch) * num_q_heads;
     if (out_dtype == TQ_F32) stage2_kernel<float><<<grid2, kHeadDim, 0, st>>>(a);
     else if (out_dtype == TQ_F16) stage2_kernel<__half><<<grid2, kHeadDim, 0, st>>>(a);
     else stage2_kernel<__nv_bfloat16><<<grid2, kHeadDim, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, int num_kv_heads)
+{
+    using namespace tq;
+    tq_layout L;
+    if (fill_layout(preset, head_dim, &L) || head_dim != kHeadDim || num_kv_heads < 1 ||
+        num_q_heads < 1 || num_q_heads % num_kv_heads)
+        return -1;
+    return mma_stage1_supported(L, num_kv_heads, num_q_heads / num_kv_heads) ? 1 : 0;
 }

@@ -1,0 +1,664 @@
+// Decode stage 1 on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate).
+//
+// Same partials as the CUDA-core stage 1 (per split: o_s and lse_s in the
+// fp32 workspace), computed per CTA = (split, sequence) over all kv heads:
+// one warp per kv head, 16-token tiles streamed into a shared-memory ring with
+// 16-byte cp.async copies of whole token rows (Hk contiguous slots each).
+//
+// Per tile and warp, with G query heads sharing the kv head:
+//   scores  S[t, g] = sum_d K^[t, d] Q[g, d]      A = K^ (16 tokens x 16 dims),
+//                                                B = q columns (16 dims x 8)
+//   values  O[d, g] += sum_t V^[t, d] P'[t, g]    A = V codes (16 dims x 16 tokens),
+//                                                B = P' columns (16 tokens x 8)
+// The grouped-query tiles are dense after unpacking, so they run as MMAs.
+// Precision: fp16 operands carry 11 bits, so every fp32 quantity that is not
+// exactly representable is split into hi = fp16(x) and lo = fp16(x - hi):
+// q (all presets), the Lloyd-Max centroids of MSE keys, and P' (for G = 4 the
+// spare 4 columns carry the lo parts; for G = 8 a second MMA does).  FP8 keys and integer value codes
+// are exact in fp16.  The value path uses P' = p * v_scale and adds
+// sum_t p_t v_zero_t separately (v_hat = code * scale + zero).
+//
+// Method sources: "vllm-project/vllm pull 38479" digest, implementation item 4
+// (split-K stage 1 / stage 2); "vllm.v1.attention.backends.turboquant_attn" API
+// page, "_decode_attention" (GQA grouping, fixed split count);
+// "turboquant-plus.md", weight pre-rotation note (<Q H, H K> = <Q, K>).
+#include "tq.h"
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+#include <cmath>
+
+namespace tq {
+namespace {
+
+struct MmaArgs {
+    const void* query;
+    const uint8_t* cache;
+    const int32_t* block_table;
+    int bt_stride;
+    const int32_t* seq_lens;
+    float qscale;            // softmax_scale * log2(e): scores in log2 units
+    int num_splits;
+    const int8_t* signs;
+    const float* centroids;
+    float* mid;              // (B, Hq, S, D+1)
+    int Hq, Hk, G, bs, bs_log2;
+    int row_bytes;           // Hk * slot
+    int smem_row;            // row_bytes padded to 16 mod 32 bytes
+    int nstages;
+    SlotGeom g;
+};
+
+constexpr int kTile = 32;   // tokens per pipeline stage (two 16-row MMA tiles)
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// hi/lo fp16 split of x: x ~= hi + lo with |x - hi - lo| ~ 2^-22 |x|
+__device__ __forceinline__ void split_f16(float x, float& hi, float& lo)
+{
+    hi = __half2float(__float2half_rn(x));
+    lo = x - hi;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+__device__ __forceinline__ void cp_async_wait_dyn(int n)
+{
+    // wait_group needs an immediate: dispatch the few stage counts in use
+    switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+    }
+}
+
+// n little-endian 32-bit words starting at the 2-byte aligned shared address p.
+// `mis` (0 or 2, uniform per warp) is p mod 4.
+template <int N>
+__device__ __forceinline__ void lds_words(const uint8_t* p, int mis, uint32_t (&w)[N])
+{
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(p - mis);
+    if (mis == 0) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = q[i];
+    } else {
+        uint32_t r[N + 1];
+#pragma unroll
+        for (int i = 0; i <= N; ++i) r[i] = q[i];
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], 16);
+    }
+}
+
+__device__ __forceinline__ float lds_f16(const uint8_t* p)
+{
+    return __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(p)));
+}
+
+// 3-bit group (32 codes in words W0..W2): nibble words of codes 0-7, 8-15,
+// 16-23, 24-31 with every nibble's top bit clear.
+__device__ __forceinline__ void nibbles3(const uint32_t (&w)[3], uint32_t (&n)[4])
+{
+    n[0] = w[0] & 0x77777777u;
+    n[1] = w[1] & 0x77777777u;
+    n[2] = w[2] & 0x77777777u;
+    n[3] = ((w[0] >> 3) & 0x11111111u) | ((w[1] >> 2) & 0x22222222u) | ((w[2] >> 1) & 0x44444444u);
+}
+
+// Token of QK row r (0..15) inside a tile.  Rows r and r+8 of a thread hold
+// tokens whose shared-memory rows are 8 apart modulo 8 (fewer bank
+// conflicts), and the four tokens 4m..4m+3 that one PV thread needs come
+// from exactly two QK threads.
+__device__ __forceinline__ int qk_token(int r)
+{
+    const int gid = r & 7, m = gid >> 1, e = gid & 1;
+    const bool second = r >= 8;
+    const bool hi_pair = (m >= 2) != second;   // +2 for (m<2, second row) or (m>=2, first row)
+    return 4 * m + e + (hi_pair ? 2 : 0);
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two_bytes)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu),
+                                                     __NV_E4M3);
+    return uint32_t(h.x) | (uint32_t(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b)
+{
+    __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c)
+{
+    __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                        *reinterpret_cast<const __half2*>(&c));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// two E4M3 pairs (low and high half of w) -> two f16x2
+__device__ __forceinline__ void cvt_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1: row gid+8).
+// Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
+template <int KMODE, int G>
+__device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
+                                        const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
+                                        const uint32_t (&T)[4][2], float (&out)[4], float (&outl)[4])
+{
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float scl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (KMODE == 8) {
+        const uint32_t* k0p = reinterpret_cast<const uint32_t*>(r0 + 4 * tig);
+        const uint32_t* k1p = reinterpret_cast<const uint32_t*>(r1 + 4 * tig);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t A[4];
+            cvt_e4m3x4(k0p[4 * kk], A[0], A[2]);
+            cvt_e4m3x4(k1p[4 * kk], A[1], A[3]);
+            mma16816(sc[kk & 1], A, bq[kk][0], bq[kk][1]);
+            if constexpr (G == 8) mma16816(scl[kk & 1], A, bql[kk][0], bql[kk][1]);
+        }
+    } else {
+        uint32_t w0[3], w1[3], c0[4], c1[4];
+        lds_words<3>(r0 + 12 * tig, kmis, w0);
+        lds_words<3>(r1 + 12 * tig, kmis, w1);
+        nibbles3(w0, c0);
+        nibbles3(w1, c1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t s0 = c0[kk >> 1] >> (16 * (kk & 1));
+            const uint32_t s1 = c1[kk >> 1] >> (16 * (kk & 1));
+            uint32_t Ahi[4], Alo[4];
+            {
+                const uint32_t p0 = prmt(T[0][0], T[0][1], s0), p1 = prmt(T[1][0], T[1][1], s0);
+                const uint32_t q0 = prmt(T[0][0], T[0][1], s1), q1 = prmt(T[1][0], T[1][1], s1);
+                Ahi[0] = prmt(p0, p1, 0x5140u);
+                Ahi[2] = prmt(p0, p1, 0x7362u);
+                Ahi[1] = prmt(q0, q1, 0x5140u);
+                Ahi[3] = prmt(q0, q1, 0x7362u);
+            }
+            {
+                const uint32_t p0 = prmt(T[2][0], T[2][1], s0), p1 = prmt(T[3][0], T[3][1], s0);
+                const uint32_t q0 = prmt(T[2][0], T[2][1], s1), q1 = prmt(T[3][0], T[3][1], s1);
+                Alo[0] = prmt(p0, p1, 0x5140u);
+                Alo[2] = prmt(p0, p1, 0x7362u);
+                Alo[1] = prmt(q0, q1, 0x5140u);
+                Alo[3] = prmt(q0, q1, 0x7362u);
+            }
+            if constexpr (G == 4) {
+                mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
+                mma16816(sc[1], Alo, bq[kk][0], bq[kk][1]);
+            } else {
+                mma16816(sc[kk & 1], Ahi, bq[kk][0], bq[kk][1]);
+                mma16816(scl[0], Ahi, bql[kk][0], bql[kk][1]);
+                mma16816(scl[1], Alo, bq[kk][0], bq[kk][1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[i] = sc[0][i] + sc[1][i];
+        outl[i] = scl[0][i] + scl[1][i];
+    }
+}
+
+// P' of one 16-row tile to the B layout of the value MMA: thread (gid, tig)
+// feeds column gid for tokens 4 tig .. 4 tig + 3, which QK threads with
+// gid 2 tig and 2 tig + 1 hold (first row = qk_token(gid), second = qk_token(gid + 8)).
+// pp[j][r]: P' of the thread's head j (G = 8: heads 2 tig, 2 tig + 1), row r.
+template <int G>
+__device__ __forceinline__ void p_to_b(const float (&pp)[G == 8 ? 2 : 1][2], int gid, int tig,
+                                       uint32_t (&pb)[2][2])
+{
+    uint32_t Xh, Yh, Xl, Yl;
+    if constexpr (G == 4) {
+        float h0, l0, h1, l1;
+        split_f16(pp[0][0], h0, l0);
+        split_f16(pp[0][1], h1, l1);
+        Xh = pack_half2(h0, h1);        // column (head, hi)
+        Yh = pack_half2(l0, l1);        // column (head, lo)
+        Xl = Yl = 0u;
+    } else {
+        float h0, l0, h1, l1, h2, l2, h3, l3;
+        split_f16(pp[0][0], h0, l0);
+        split_f16(pp[0][1], h1, l1);
+        split_f16(pp[1][0], h2, l2);
+        split_f16(pp[1][1], h3, l3);
+        Xh = pack_half2(h0, h1);
+        Yh = pack_half2(h2, h3);
+        Xl = pack_half2(l0, l1);
+        Yl = pack_half2(l2, l3);
+    }
+    const int src_tig = gid >> 1;
+    const bool take_y = gid & 1;
+    const int srcA = 4 * (2 * tig) + src_tig, srcB = 4 * (2 * tig + 1) + src_tig;
+    constexpr int NP = G == 4 ? 1 : 2;
+#pragma unroll
+    for (int part = 0; part < NP; ++part) {
+        const uint32_t X = part ? Xl : Xh, Y = part ? Yl : Yh;
+        const uint32_t ax = __shfl_sync(0xffffffffu, X, srcA), ay = __shfl_sync(0xffffffffu, Y, srcA);
+        const uint32_t bx = __shfl_sync(0xffffffffu, X, srcB), by = __shfl_sync(0xffffffffu, Y, srcB);
+        const uint32_t XA = take_y ? ay : ax, XB = take_y ? by : bx;
+        if (tig < 2) { pb[part][0] = prmt(XA, XB, 0x5410u); pb[part][1] = prmt(XA, XB, 0x7632u); }
+        else         { pb[part][0] = prmt(XA, XB, 0x7632u); pb[part][1] = prmt(XA, XB, 0x5410u); }
+    }
+}
+
+// Value MMAs of one 16-row tile: tokens 4 tig + j of the tile, dims 16 gid + 2i (+1).
+template <int VBITS, int G>
+__device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, int tig, int vmis,
+                                        const uint32_t (&pb)[2][2], float (&acc)[8][4])
+{
+    const uint32_t kMagic = 0x64006400u;       // half2(1024, 1024)
+    const uint32_t kSixteenth = 0x2C002C00u;   // half2(1/16, 1/16)
+    const uint32_t kMinus64 = 0xD400D400u;     // half2(-64, -64)
+    uint32_t vw[4][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint8_t* rv = tile_v + (4 * tig + j) * rs;
+        if constexpr (VBITS == 4) {
+            lds_words<2>(rv + 8 * gid, vmis, vw[j]);
+        } else {
+            uint32_t w[3], n[4];
+            lds_words<3>(rv + 12 * (gid >> 1), vmis, w);
+            nibbles3(w, n);
+            vw[j][0] = (gid & 1) ? n[2] : n[0];
+            vw[j][1] = (gid & 1) ? n[3] : n[1];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t sel = uint32_t(i & 3) | (uint32_t((i & 3) + 4) << 8);
+        const uint32_t zab = prmt(vw[0][i >> 2], vw[1][i >> 2], sel);
+        const uint32_t zcd = prmt(vw[2][i >> 2], vw[3][i >> 2], sel);
+        const uint32_t A[4] = {hsub2_u((zab & 0x000F000Fu) | kMagic, kMagic),
+                               hfma2_u((zab & 0x00F000F0u) | kMagic, kSixteenth, kMinus64),
+                               hsub2_u((zcd & 0x000F000Fu) | kMagic, kMagic),
+                               hfma2_u((zcd & 0x00F000F0u) | kMagic, kSixteenth, kMinus64)};
+        mma16816(acc[i], A, pb[0][0], pb[0][1]);
+        if constexpr (G == 8) mma16816(acc[i], A, pb[1][0], pb[1][1]);
+    }
+}
+
+// KMODE: 8 = FP8 E4M3 keys, 3 = 3-bit Lloyd-Max keys.  VBITS: 3 or 4.
+// G: 4 (columns = 4 heads x {hi, lo}) or 8 (columns = 8 heads).
+// One CTA = (split, sequence); warp w = kv head w; each iteration consumes a
+// 32-token tile (two 16-row MMA tiles) with one softmax update.
+template <typename TQ, int KMODE, int VBITS, int G>
+__global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int split = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h = warp;
+    const int S = a.num_splits, Hk = a.Hk, Hq = a.Hq, Greal = a.G;
+    const int nwarps = blockDim.x >> 5;
+
+    const int L = a.seq_lens[b];
+    int chunk = (L + S - 1) / S;
+    chunk = (chunk + kTile - 1) / kTile * kTile;
+    const int t_begin = split * chunk;
+    const int t_end = min(L, t_begin + chunk);
+
+    if (t_begin >= t_end) {      // empty split: lse = -inf and a zero partial
+        for (int i = threadIdx.x; i < Hk * Greal * (kHeadDim + 1); i += blockDim.x) {
+            const int hq = i / (kHeadDim + 1), d = i % (kHeadDim + 1);
+            float* m = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
+            m[d] = d == kHeadDim ? -INFINITY : 0.f;
+        }
+        return;
+    }
+
+    // ---------------- q columns: B operand of the score MMA.  Each warp
+    // rotates (MSE keys) and scales its G query heads with lane l holding dims
+    // 4l..4l+3, parks them in the (still empty) ring, and every thread reads
+    // back the 32 values of its column.  The k index of k-step kk and thread
+    // tig maps to dims
+    //   FP8 keys:   16 kk + 4 tig + j   one key word per k-step, bank-conflict
+    //               free across the warp
+    //   3-bit keys: 32 tig + 4 kk + j   one 32-code group (three words) per thread
+    uint32_t bq[8][2], bql[8][2];
+    {
+        float* sq = reinterpret_cast<float*>(smem) + h * G * kHeadDim;
+        float sgn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sgn[i] = KMODE == 8 ? 1.f : float(a.signs[4 * lane + i]);
+        const TQ* Q = static_cast<const TQ*>(a.query);
+        for (int g = 0; g < G; ++g) {
+            float qv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (g < Greal) {        // warp-uniform
+                const TQ* qp = Q + ((long long)b * Hq + h * Greal + g) * kHeadDim + 4 * lane;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qv[i] = sgn[i] * to_f32(qp[i]);
+                if constexpr (KMODE != 8) {
+                    fwht128_warp(qv, lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) qv[i] *= 0.08838834764831845f;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qv[i] *= a.qscale;
+            }
+            reinterpret_cast<float4*>(sq + g * kHeadDim)[lane] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+        }
+        __syncwarp();
+        const int col_head = G == 4 ? (gid >> 1) : gid;
+        const bool col_lo = G == 4 && (gid & 1);
+        const float* qc = sq + col_head * kHeadDim;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const float4 x = reinterpret_cast<const float4*>(qc + (KMODE == 8 ? 16 * kk + 4 * tig : 32 * tig + 4 * kk))[0];
+            float hi[4], lo[4];
+            split_f16(x.x, hi[0], lo[0]);
+            split_f16(x.y, hi[1], lo[1]);
+            split_f16(x.z, hi[2], lo[2]);
+            split_f16(x.w, hi[3], lo[3]);
+            if (G == 4) {
+                bq[kk][0] = col_lo ? pack_half2(lo[0], lo[1]) : pack_half2(hi[0], hi[1]);
+                bq[kk][1] = col_lo ? pack_half2(lo[2], lo[3]) : pack_half2(hi[2], hi[3]);
+                bql[kk][0] = bql[kk][1] = 0u;
+            } else {
+                bq[kk][0] = pack_half2(hi[0], hi[1]);
+                bq[kk][1] = pack_half2(hi[2], hi[3]);
+                bql[kk][0] = pack_half2(lo[0], lo[1]);
+                bql[kk][1] = pack_half2(lo[2], lo[3]);
+            }
+        }
+        __syncthreads();            // the ring is about to receive the first tiles
+    }
+
+    // ---------------- centroid byte planes for the PRMT lookup (3-bit keys):
+    // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
+    // fp16 residual c - fp16(c); [k >> 2] holds entries 4(k>>2) .. 4(k>>2)+3.
+    uint32_t T[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+    if constexpr (KMODE == 3) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float c = a.centroids[k];
+            const __half chi = __float2half_rn(c);
+            const __half clo = __float2half_rn(c - __half2float(chi));
+            const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
+            const int sh = 8 * (k & 3);
+            T[0][k >> 2] |= (hb & 0xFFu) << sh;
+            T[1][k >> 2] |= (hb >> 8) << sh;
+            T[2][k >> 2] |= (lb & 0xFFu) << sh;
+            T[3][k >> 2] |= (lb >> 8) << sh;
+        }
+    }
+
+    // ---------------- shared-memory ring of 32 token rows (all kv heads)
+    const int row_bytes = a.row_bytes;        // global token row (Hk slots)
+    const int rs = a.smem_row;                // shared row stride: 16 mod 32 bytes
+    const int stage_bytes = kTile * rs;
+    const int NST = a.nstages;
+    const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
+    const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
+    const int per_row = row_bytes >> 4;
+    const int lg = a.bs_log2;
+    auto issue = [&](int tile) {
+        if (tile < ntiles) {
+            uint8_t* dst = smem + (tile % NST) * stage_bytes;
+            const int tbase = t_begin + tile * kTile;
+            for (int r = warp; r < kTile; r += nwarps) {   // one warp per token row
+                const int t = tbase + r;
+                const long long page = bt[t >> lg];
+                const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes;
+                uint8_t* d = dst + r * rs;
+                for (int k = lane; k < per_row; k += 32) cp_async16(d + 16 * k, src + 16 * k);
+            }
+        }
+        cp_async_commit();
+    };
+    for (int i = 0; i < NST - 1; ++i) issue(i);
+
+    constexpr int NH = G == 8 ? 2 : 1;        // query heads per thread (softmax state)
+    float m_run[NH], l_run[NH], z_run[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) { m_run[j] = -INFINITY; l_run[j] = 0.f; z_run[j] = 0.f; }
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+    const int tau0 = qk_token(gid), tau1 = qk_token(gid + 8);
+    const int hoff = h * a.g.slot;
+    const int kmis = hoff & 2;
+    const int vmis = (hoff + a.g.off_v_data) & 2;
+
+    for (int it = 0; it < ntiles; ++it) {
+        cp_async_wait_dyn(NST - 2);    // tile `it` has landed (this thread's copies)
+        __syncthreads();               // ... everyone's; and tile it-1's stage is free
+        issue(it + NST - 1);
+        const uint8_t* st = smem + (it % NST) * stage_bytes + hoff;
+        const int t0 = t_begin + it * kTile;
+
+        // ---- scores of both 16-row tiles
+        float s[NH][2][2], vs[2][2], vz[2][2];
+        bool ok[2][2];
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+            const uint8_t* r0 = st + (16 * rt + tau0) * rs;
+            const uint8_t* r1 = st + (16 * rt + tau1) * rs;
+            float sc[4], scl[4];
+            qk_tile<KMODE, G>(r0, r1, tig, kmis, bq, bql, T, sc, scl);
+            float n0 = 1.f, n1 = 1.f;
+            if constexpr (KMODE == 3) { n0 = lds_f16(r0 + a.g.off_k_norm); n1 = lds_f16(r1 + a.g.off_k_norm); }
+            vs[rt][0] = lds_f16(r0 + a.g.off_v_scale);
+            vz[rt][0] = lds_f16(r0 + a.g.off_v_zero);
+            vs[rt][1] = lds_f16(r1 + a.g.off_v_scale);
+            vz[rt][1] = lds_f16(r1 + a.g.off_v_zero);
+            ok[rt][0] = t0 + 16 * rt + tau0 < t_end;
+            ok[rt][1] = t0 + 16 * rt + tau1 < t_end;
+            if constexpr (G == 4) {
+                s[0][rt][0] = (sc[0] + sc[1]) * n0;
+                s[0][rt][1] = (sc[2] + sc[3]) * n1;
+            } else {
+                s[0][rt][0] = (sc[0] + scl[0]) * n0;
+                s[1][rt][0] = (sc[1] + scl[1]) * n0;
+                s[0][rt][1] = (sc[2] + scl[2]) * n1;
+                s[1][rt][1] = (sc[3] + scl[3]) * n1;
+            }
+        }
+
+        // ---- one online-softmax update for the 32 tokens (log2 units)
+        float pp[2][NH][2];   // [row tile][head][row]: P' = p * v_scale
+        float alpha[NH];
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            float mt = -INFINITY;
+#pragma unroll
+            for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (!ok[rt][r]) s[j][rt][r] = -INFINITY;
+                    mt = fmaxf(mt, s[j][rt][r]);
+                }
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+            const float mn = fmaxf(m_run[j], mt);        // finite: the tile's first token is valid
+            alpha[j] = fast_exp2(m_run[j] - mn);
+            float lsum = 0.f, zsum = 0.f;
+#pragma unroll
+            for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float p = fast_exp2(s[j][rt][r] - mn);   // 0 for masked rows
+                    lsum += p;
+                    zsum += ok[rt][r] ? p * vz[rt][r] : 0.f;
+                    pp[rt][j][r] = ok[rt][r] ? p * vs[rt][r] : 0.f;
+                }
+            l_run[j] = l_run[j] * alpha[j] + lsum;
+            z_run[j] = z_run[j] * alpha[j] + zsum;
+            m_run[j] = mn;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (G == 4) {
+                acc[i][0] *= alpha[0]; acc[i][1] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][3] *= alpha[0];
+            } else {
+                acc[i][0] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][1] *= alpha[1]; acc[i][3] *= alpha[1];
+            }
+        }
+
+        // ---- values
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+            uint32_t pb[2][2];
+            p_to_b<G>(pp[rt], gid, tig, pb);
+            pv_tile<VBITS, G>(st + 16 * rt * rs + a.g.off_v_data, rs, gid, tig, vmis, pb, acc);
+        }
+    }
+    cp_async_wait<0>();
+
+    // ---------------- epilogue: finish the row sums, write o_s and lse_s
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+#pragma unroll
+        for (int m = 4; m < 32; m <<= 1) {
+            l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], m);
+            z_run[j] += __shfl_xor_sync(0xffffffffu, z_run[j], m);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+        const int g = G == 4 ? tig : 2 * tig + j;
+        if (g >= Greal) continue;
+        const int hq = h * Greal + g;
+        float* mp = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
+        const float inv = 1.f / l_run[j];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int d = 16 * gid + 2 * i;
+            float e, o;
+            if constexpr (G == 4) { e = acc[i][0] + acc[i][1]; o = acc[i][2] + acc[i][3]; }
+            else { e = j == 0 ? acc[i][0] : acc[i][1]; o = j == 0 ? acc[i][2] : acc[i][3]; }
+            mp[d] = (e + z_run[j]) * inv;
+            mp[d + 1] = (o + z_run[j]) * inv;
+        }
+        if (gid == 0) mp[kHeadDim] = (m_run[j] + log2f(l_run[j])) * 0.6931471805599453f;
+    }
+}
+
+template <typename TQ, int KMODE, int VBITS, int G>
+cudaError_t launch_t(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
+{
+    auto k = stage1_mma_kernel<TQ, KMODE, VBITS, G>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.num_splits, B);
+    k<<<grid, 32 * a.Hk, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename TQ, int KMODE, int VBITS>
+cudaError_t launch_g(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
+{
+    return a.G <= 4 ? launch_t<TQ, KMODE, VBITS, 4>(a, B, smem, st)
+                    : launch_t<TQ, KMODE, VBITS, 8>(a, B, smem, st);
+}
+
+template <typename TQ>
+cudaError_t launch_q(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
+{
+    if (a.g.key_fp8) return launch_g<TQ, 8, 4>(a, B, smem, st);
+    if (a.g.value_bits == 4) return launch_g<TQ, 3, 4>(a, B, smem, st);
+    return launch_g<TQ, 3, 3>(a, B, smem, st);
+}
+
+}  // namespace
+
+bool mma_stage1_supported(const tq_layout& L, int num_kv_heads, int group)
+{
+    const bool keys_ok = (L.key_fp8 && L.value_bits == 4) || (!L.key_fp8 && L.key_bits == 3);
+    const bool vals_ok = L.value_bits == 3 || L.value_bits == 4;
+    const int row = num_kv_heads * L.slot_size_aligned;
+    return keys_ok && vals_ok && num_kv_heads >= 1 && num_kv_heads <= 16 && group >= 1 &&
+           group <= 8 && row % 16 == 0 && 2 * kTile * (row + 16) <= 110 * 1024;
+}
+
+int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const uint8_t* kv_cache,
+                      const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                      float softmax_scale, int num_splits, const int8_t* signs,
+                      const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
+                      cudaStream_t st)
+{
+    MmaArgs a;
+    a.query = query;
+    a.cache = kv_cache;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.seq_lens = seq_lens;
+    a.qscale = softmax_scale * 1.4426950408889634f;
+    a.num_splits = num_splits;
+    a.signs = signs;
+    a.centroids = centroids;
+    a.mid = mid;
+    a.Hq = Hq;
+    a.Hk = Hk;
+    a.G = Hq / Hk;
+    a.bs = bs;
+    a.bs_log2 = bs == 16 ? 4 : bs == 32 ? 5 : bs == 64 ? 6 : 7;
+    a.row_bytes = Hk * L.slot_size_aligned;
+    // a shared row stride of 16 mod 32 bytes (4 mod 8 words) puts the rows a
+    // warp reads in the same instruction on distinct bank quads
+    a.smem_row = (a.row_bytes % 32 == 0) ? a.row_bytes + 16 : a.row_bytes;
+    a.g = geom_of(L);
+    const int stage = kTile * a.smem_row;
+    int nst = (100 * 1024) / stage;          // ~100 KB of ring: two CTAs per SM
+    nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
+    // the q staging at kernel start borrows the ring: Hk * (4 or 8) heads * 512 B
+    while (nst * stage < Hk * (a.G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
+    a.nstages = nst;
+    const size_t smem = size_t(nst) * stage;
+    cudaError_t e = q_dtype == TQ_F16 ? launch_q<__half>(a, B, smem, st)
+                                      : launch_q<__nv_bfloat16>(a, B, smem, st);
+    return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace tq

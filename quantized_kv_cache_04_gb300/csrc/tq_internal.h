@@ -5,6 +5,7 @@
 #include "tq.h"
 
 #include <cstdint>
+#include <cuda_runtime.h>
 
 namespace tq {
 
@@ -41,5 +42,13 @@ inline SlotGeom geom_of(const tq_layout& L)
     g.slot = L.slot_size_aligned;
     return g;
 }
+
+// Tensor-core stage 1 (tq_decode_mma.cu): which shapes it serves, and its launcher.
+bool mma_stage1_supported(const tq_layout& L, int num_kv_heads, int group);
+int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const uint8_t* kv_cache,
+                      const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                      float softmax_scale, int num_splits, const int8_t* signs,
+                      const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
+                      cudaStream_t st);
 
 }  // namespace tq

@@ -49,15 +49,22 @@ __device__ __forceinline__ void pack_codes(uint8_t* dst, const int (&c)[4], int 
     } else if constexpr (BITS == 2) {   // lane pairs form 16 bits
         const uint32_t hi = __shfl_down_sync(0xffffffffu, w, 1);
         if (!(lane & 1)) d16[lane >> 1] = uint16_t(w | (hi << 8));
-    } else {                            // 3 bits: groups of 4 lanes form 48 bits = 3 words
+    } else {
+        // 3 bits, 32-code groups of three 32-bit words W0..W2: code 8w+i in
+        // bits [4i, 4i+3) of Ww (i < 8, w < 3), bit w of code 24+i in bit
+        // 4i+3 of Ww.  Lanes 8g..8g+7 hold group g; lanes 8g+6, 8g+7 hold
+        // codes 24..31, whose bits ride in the nibble tops written by lanes
+        // 8g..8g+5 (lane 8g+2w+h writes half h of Ww).
         static_assert(BITS == 3, "2, 3 or 4 bits");
-        const int g = lane & ~3, r = lane & 3;
-        const uint64_t w0 = __shfl_sync(0xffffffffu, w, g);
-        const uint64_t w1 = __shfl_sync(0xffffffffu, w, g + 1);
-        const uint64_t w2 = __shfl_sync(0xffffffffu, w, g + 2);
-        const uint64_t w3 = __shfl_sync(0xffffffffu, w, g + 3);
-        const uint64_t bits = w0 | (w1 << 12) | (w2 << 24) | (w3 << 36);
-        if (r < 3) d16[3 * (g >> 2) + r] = uint16_t(bits >> (16 * r));
+        const int j = lane & 7, h = j & 1, w3 = j >> 1;
+        const uint32_t spill = __shfl_sync(0xffffffffu, w, (lane & ~7) + 6 + h);
+        if (j < 6) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v |= ((uint32_t(c[i]) & 7u) | (((spill >> (3 * i + w3)) & 1u) << 3)) << (4 * i);
+            d16[6 * (lane >> 3) + 2 * w3 + h] = uint16_t(v);
+        }
     }
 }
 

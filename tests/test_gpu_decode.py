@@ -34,14 +34,31 @@ def _gpu_decode(preset, q, cache_np, bt, seq_lens, Hk, bs, signs, c32, num_split
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-CASES = [  # (G, Hk, bs, seq_lens, splits)
+CASES = [  # (G, Hk, bs, seq_lens, splits): CUDA-core and tensor-core stage 1 shapes
     (4, 2, 16, [512], 0),
     (8, 2, 64, [1000, 1, 0, 130], 7),
     (1, 4, 32, [65, 300], 1),
     (16, 1, 128, [1500], 64),
     (6, 2, 16, [33, 200], 3),
     (4, 8, 32, [17, 0, 256, 97, 5], 0),
+    (8, 8, 64, [700, 65, 1], 3),
+    (4, 8, 16, [1024, 31], 0),
+    (1, 8, 32, [129, 16], 2),
+    (2, 8, 128, [1000], 64),
+    (6, 8, 16, [250, 0], 5),
+    (5, 16, 32, [90, 333], 0),
+    (16, 8, 16, [200], 2),
 ]
+
+
+def _expected_kind(preset, G, Hk):
+    """Tensor-core stage 1 serves FP8 / 3-bit keys, G <= 8, Hk <= 16 and
+    token rows that are whole 16-byte units and fit a two-stage ring of 32
+    rows in ~110 KB of shared memory."""
+    slot = [196, 134, 118, 102][preset]
+    row = Hk * slot
+    return int(preset != 1 and G <= 8 and Hk <= 16 and row % 16 == 0
+               and 2 * 32 * (row + 16) <= 110 * 1024)
 
 
 @pytest.mark.parametrize("preset", PRESETS)
@@ -49,6 +66,7 @@ CASES = [  # (G, Hk, bs, seq_lens, splits)
 @pytest.mark.parametrize("qdtype", [torch.float16, torch.bfloat16])
 def test_decode_on_oracle_cache(orc, preset, case, qdtype):
     G, Hk, bs, seq_lens, S = CASES[case]
+    assert tq.tq_decode_kernel_kind(preset, 128, G * Hk, Hk) == _expected_kind(preset, G, Hk)
     rng = np.random.default_rng(1000 * preset + 10 * case + (qdtype == torch.bfloat16))
     pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng,
                        dtype="bfloat16" if qdtype == torch.bfloat16 else "float16")
@@ -111,11 +129,13 @@ def test_end_to_end_store_then_decode(orc, preset):
     check_decode(o, l, ref_o, ref_l, f"e2e preset {preset}")
 
 
-def test_planted_key_peaked_softmax(orc):
+@pytest.mark.parametrize("preset,Hk", [(3, 2), (3, 8), (2, 8), (0, 8)])
+def test_planted_key_peaked_softmax(orc, preset, Hk):
     """A key aligned with the query (logit ~ 12) dominates each split: the
-    LSE merge of peaked partials stays within 1e-4."""
-    rng = np.random.default_rng(4)
-    preset, Hk, G, bs, n = 3, 2, 4, 128, 8192
+    LSE merge of peaked partials stays within 1e-4 (this is where fp16
+    rounding of centroids or q alone would miss the bar)."""
+    rng = np.random.default_rng(4 + preset + Hk)
+    G, bs, n = 4, 128, 8192 if Hk == 2 else 4096
     pb = paged_problem(orc, preset, [n], Hk, bs, rng, dtype="bfloat16")
     q = torch.from_numpy(rng.normal(size=(1, G * Hk, 128)) * 1.2).to(torch.bfloat16)
     # plant keys aligned with head-0 queries every 1024 tokens, re-store with the oracle
