@@ -180,6 +180,34 @@ int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,
                         void* out, int out_dtype, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* tq_decode_attention without a caller-supplied workspace.  The pages have
+ * no counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory, for example a serving engine that gives nearly all
+ * device memory to its own KV-cache pool at start-up and treats any later
+ * cudaMalloc as a failure, or a host loop that must not take cudaMalloc's
+ * implicit device-wide synchronisation.  The split partials go to an array of
+ * TQ_NOALLOC_SCRATCH_BYTES that the library declares in device memory (every
+ * GPU that loads the library holds it until the process exits); this call
+ * allocates nothing.  Arguments and results are those of tq_decode_attention
+ * minus workspace/workspace_bytes.  num_splits = 0 picks as
+ * tq_decode_pick_splits does, lowered until B*Hq*S*(D+1)*4 bytes fit; an
+ * explicit num_splits whose partials exceed the array returns
+ * TQ_ERR_WORKSPACE, as does a shape for which even one split does not fit.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and leave the
+ * last call's partials in it (nothing in it has to start at zero): calls
+ * whose kernels overlap on the GPU, e.g. on two streams at once, race. */
+#define TQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int tq_decode_attention_noalloc(int preset, int head_dim, int batch, int num_q_heads,
+                                int num_kv_heads, int block_size, int q_dtype, const void* query,
+                                const uint8_t* kv_cache, long long num_blocks,
+                                const int32_t* block_table, int block_table_stride,
+                                const int32_t* seq_lens, int max_seq_len,
+                                float softmax_scale, int num_splits,
+                                const int8_t* signs, const float* centroids,
+                                void* out, int out_dtype, float* lse, void* stream);
+
 /* Which stage-1 kernel tq_decode_attention runs for this shape (host only):
  * 1 = tensor-core stage 1 (FP8 or 3-bit keys, 3/4-bit values, group size
  * <= 8, num_kv_heads <= 16, token row = num_kv_heads * slot a multiple of 16

@@ -187,3 +187,21 @@ def decode_attention(preset: int, query, kv_cache, block_table, seq_lens, max_se
                              _stream_ptr(stream))
     if rc:
         raise TQError("tq_decode_attention", rc)
+
+
+TQ_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def tq_decode_attention_noalloc(*args) -> int:
+    """Raw C call of the decode entry point that allocates nothing (arguments
+    as tq_decode_attention without workspace and workspace_bytes).  For
+    callers that cannot allocate device memory: the split partials live in a
+    fixed 16 MiB array the library declares in device memory, shared by all
+    calls, so calls that overlap on the GPU race.  Returns the status."""
+    L = load()
+    fn = L.tq_decode_attention_noalloc
+    if fn.argtypes is None:
+        fn.argtypes = ([_c_int] * 7 + [_c_vp, _c_vp, _c_ll, _c_vp, _c_int, _c_vp, _c_int,
+                                       ctypes.c_float, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_vp,
+                                       _c_vp])
+    return fn(*args)
