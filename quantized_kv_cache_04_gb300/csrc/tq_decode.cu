@@ -217,27 +217,49 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
     }
 }
 
+// Stage 2: one warp per (sequence, query head).  Lanes take the splits' LSEs
+// for the max and the weight sum; then each lane owns 4 of the 128 dims and
+// accumulates the weighted split outputs (independent loads across splits).
+constexpr int kStage2Warps = 4;
+
 template <typename TO>
-__global__ void __launch_bounds__(kHeadDim) stage2_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(32 * kStage2Warps) stage2_kernel(DecodeArgs a)
 {
-    const long long bh = blockIdx.x;   // b * Hq + hq
-    const int d = threadIdx.x, S = a.num_splits;
+    const int lane = threadIdx.x & 31;
+    const long long bh = (long long)blockIdx.x * kStage2Warps + (threadIdx.x >> 5);   // b * Hq + hq
+    if (bh >= (long long)a.B * a.Hq) return;
+    const int S = a.num_splits;
     const float* mp = a.mid + bh * S * (kHeadDim + 1);
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, mp[s * (kHeadDim + 1) + kHeadDim]);
-    float W = 0.f, o = 0.f;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, mp[s * (kHeadDim + 1) + kHeadDim]);
+    M = warp_max(M);
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    float W = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
-            const float ls = mp[s * (kHeadDim + 1) + kHeadDim];
-            if (ls == -INFINITY) continue;
-            const float w = expf(ls - M);
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const int s = s0 + lane;
+            const float ls = s < S ? mp[s * (kHeadDim + 1) + kHeadDim] : -INFINITY;
+            const float w = ls == -INFINITY ? 0.f : expf(ls - M);
             W += w;
-            o += w * mp[s * (kHeadDim + 1) + d];
+            const int n = min(32, S - s0);
+            for (int j = 0; j < n; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+                if (wj != 0.f) {                       // warp-uniform: skips empty splits
+                    const float* row = mp + (s0 + j) * (kHeadDim + 1) + 4 * lane;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] += wj * row[i];
+                }
+            }
         }
-        o /= W;
+        W = warp_sum(W);
+        const float inv = 1.f / W;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] *= inv;
     }
-    static_cast<TO*>(a.out)[bh * kHeadDim + d] = from_f32<TO>(o);
-    if (d == 0 && a.lse) a.lse[bh] = M == -INFINITY ? -INFINITY : M + logf(W);
+    TO* out = static_cast<TO*>(a.out) + bh * kHeadDim + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = from_f32<TO>(o[i]);
+    if (lane == 0 && a.lse) a.lse[bh] = M == -INFINITY ? -INFINITY : M + logf(W);
 }
 
 template <typename TQ, bool FP8, int KB, int VB>
@@ -330,10 +352,11 @@ extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_
                                           : launch_stage1<__nv_bfloat16>(preset, a, st);
         if (e != cudaSuccess) return TQ_ERR_CUDA;
     }
-    const unsigned grid2 = unsigned(batch) * num_q_heads;
-    if (out_dtype == TQ_F32) stage2_kernel<float><<<grid2, kHeadDim, 0, st>>>(a);
-    else if (out_dtype == TQ_F16) stage2_kernel<__half><<<grid2, kHeadDim, 0, st>>>(a);
-    else stage2_kernel<__nv_bfloat16><<<grid2, kHeadDim, 0, st>>>(a);
+    const unsigned rows = unsigned(batch) * num_q_heads;
+    const unsigned grid2 = (rows + kStage2Warps - 1) / kStage2Warps;
+    if (out_dtype == TQ_F32) stage2_kernel<float><<<grid2, 32 * kStage2Warps, 0, st>>>(a);
+    else if (out_dtype == TQ_F16) stage2_kernel<__half><<<grid2, 32 * kStage2Warps, 0, st>>>(a);
+    else stage2_kernel<__nv_bfloat16><<<grid2, 32 * kStage2Warps, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

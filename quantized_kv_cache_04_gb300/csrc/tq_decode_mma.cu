@@ -2,8 +2,9 @@
 //
 // Same partials as the CUDA-core stage 1 (per split: o_s and lse_s in the
 // fp32 workspace), computed per CTA = (split, sequence) over all kv heads:
-// one warp per kv head, 16-token tiles streamed into a shared-memory ring with
-// 16-byte cp.async copies of whole token rows (Hk contiguous slots each).
+// one warp per kv head, 32-token tiles streamed into a shared-memory ring by
+// bulk (TMA) copies of whole token rows (Hk contiguous slots each) whose
+// completion is tracked by mbarriers with bounded waits.
 //
 // Per tile and warp, with G query heads sharing the kv head:
 //   scores  S[t, g] = sum_d K^[t, d] Q[g, d]      A = K^ (16 tokens x 16 dims),
@@ -50,6 +51,7 @@ struct MmaArgs {
 };
 
 constexpr int kTile = 32;   // tokens per pipeline stage (two 16-row MMA tiles)
+constexpr uint32_t kWaitLimit = 1u << 24;   // mbarrier polls before a stage wait gives up
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
@@ -80,27 +82,49 @@ __device__ __forceinline__ void split_f16(float x, float& hi, float& lo)
     lo = x - hi;
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+// ---- bulk (TMA) copies into shared memory, completion tracked by mbarriers
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
-    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-__device__ __forceinline__ void cp_async_wait_dyn(int n)
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {
-    // wait_group needs an immediate: dispatch the few stage counts in use
-    switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    default: cp_async_wait<7>(); break;
-    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity, giving up after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit)
+{
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // n little-endian 32-bit words starting at the 2-byte aligned shared address p.
@@ -432,28 +456,47 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
     }
 
-    // ---------------- shared-memory ring of 32 token rows (all kv heads)
+    // ---------------- shared-memory ring of 32 token rows (all kv heads),
+    // filled by bulk (TMA) copies.  Rows of one page are contiguous in global
+    // memory: one copy per page segment when the shared row stride equals the
+    // global one, else one copy per row (issued by the 32 lanes of warp 0).
     const int row_bytes = a.row_bytes;        // global token row (Hk slots)
     const int rs = a.smem_row;                // shared row stride: 16 mod 32 bytes
     const int stage_bytes = kTile * rs;
     const int NST = a.nstages;
     const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
     const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
-    const int per_row = row_bytes >> 4;
     const int lg = a.bs_log2;
+    const int seg_rows = kTile < (1 << lg) ? kTile : (1 << lg);   // rows per page segment
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * stage_bytes);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // Only rows of tokens < L are copied: block-table entries past the
+    // sequence's last page are never read.  Skipped rows keep stale bytes and
+    // are masked out of the softmax.
     auto issue = [&](int tile) {
-        if (tile < ntiles) {
-            uint8_t* dst = smem + (tile % NST) * stage_bytes;
-            const int tbase = t_begin + tile * kTile;
-            for (int r = warp; r < kTile; r += nwarps) {   // one warp per token row
-                const int t = tbase + r;
-                const long long page = bt[t >> lg];
-                const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes;
-                uint8_t* d = dst + r * rs;
-                for (int k = lane; k < per_row; k += 32) cp_async16(d + 16 * k, src + 16 * k);
-            }
+        if (tile >= ntiles || warp != 0) return;
+        uint8_t* dst = smem + (tile % NST) * stage_bytes;
+        uint64_t* bar = &full[tile % NST];
+        const int tbase = t_begin + tile * kTile;
+        const bool per_segment = rs == row_bytes;
+        const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile
+        const int seg_len = per_segment ? seg_rows : 1;               // rows per copy
+        const int nlive = min(nseg, (L - tbase + seg_len - 1) / seg_len);
+        if (lane == 0) {
+            fence_async_shared();             // prior generic reads of this stage before the async writes
+            mbar_expect_tx(bar, uint32_t(nlive * seg_len * row_bytes));
         }
-        cp_async_commit();
+        __syncwarp();
+        if (lane < nlive) {
+            const int t = tbase + lane * seg_len;
+            const long long page = bt[t >> lg];
+            const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes;
+            bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * row_bytes), bar);
+        }
     };
     for (int i = 0; i < NST - 1; ++i) issue(i);
 
@@ -470,10 +513,13 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     const int kmis = hoff & 2;
     const int vmis = (hoff + a.g.off_v_data) & 2;
 
+    int failed_at = -1;
     for (int it = 0; it < ntiles; ++it) {
-        cp_async_wait_dyn(NST - 2);    // tile `it` has landed (this thread's copies)
-        __syncthreads();               // ... everyone's; and tile it-1's stage is free
-        issue(it + NST - 1);
+        // tile `it` has landed; a copy that never completes ends the split
+        // with a NaN lse instead of hanging (bounded wait)
+        const bool ok_wait = mbar_wait(&full[it % NST], uint32_t((it / NST) & 1), kWaitLimit);
+        if (__syncthreads_or(!ok_wait)) { failed_at = it; break; }
+        issue(it + NST - 1);           // refills the stage of tile it-1: all warps are past it
         const uint8_t* st = smem + (it % NST) * stage_bytes + hoff;
         const int t0 = t_begin + it * kTile;
 
@@ -554,7 +600,15 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             pv_tile<VBITS, G>(st + 16 * rt * rs + a.g.off_v_data, rs, gid, tig, vmis, pb, acc);
         }
     }
-    cp_async_wait<0>();
+    if (failed_at >= 0) {
+        // let the copies still in flight (tiles failed_at .. failed_at + NST - 2)
+        // land, with the same bounded wait, before the CTA exits
+        for (int it = failed_at; it < min(ntiles, failed_at + NST - 1); ++it)
+            mbar_wait(&full[it % NST], uint32_t((it / NST) & 1), kWaitLimit);
+        for (int i = threadIdx.x; i < Hk * Greal; i += blockDim.x)
+            a.mid[(((long long)b * Hq + i) * S + split) * (kHeadDim + 1) + kHeadDim] = __int_as_float(0x7fc00000);
+        return;
+    }
 
     // ---------------- epilogue: finish the row sums, write o_s and lse_s
 #pragma unroll
@@ -655,7 +709,7 @@ int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const 
     // the q staging at kernel start borrows the ring: Hk * (4 or 8) heads * 512 B
     while (nst * stage < Hk * (a.G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
     a.nstages = nst;
-    const size_t smem = size_t(nst) * stage;
+    const size_t smem = size_t(nst) * stage + 8 * size_t(nst);   // ring + one mbarrier per stage
     cudaError_t e = q_dtype == TQ_F16 ? launch_q<__half>(a, B, smem, st)
                                       : launch_q<__nv_bfloat16>(a, B, smem, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
