@@ -135,11 +135,18 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def kernel_source_hash() -> str:
+    """Hash of the decode kernels' sources (both stages, both stage-1 paths)."""
+    h = hashlib.sha256()
+    for f in ("tq_decode.cu", "tq_decode_mma.cu"):
+        h.update(open(os.path.join(ROOT, "quantized_kv_cache_04_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def _traffic(workload: str, kernel: str):
     """DRAM bytes per launch from a committed ncu summary, if the kernel source
     it was taken on is the one being timed (else null)."""
-    src = os.path.join(ROOT, "quantized_kv_cache_04_gb300", "csrc", "tq_decode.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_hash()
     f = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(f):
         return None

@@ -242,13 +242,23 @@ __global__ void __launch_bounds__(32 * kStage2Warps) stage2_kernel(DecodeArgs a)
             const float w = ls == -INFINITY ? 0.f : expf(ls - M);
             W += w;
             const int n = min(32, S - s0);
-            for (int j = 0; j < n; ++j) {
-                const float wj = __shfl_sync(0xffffffffu, w, j);
-                if (wj != 0.f) {                       // warp-uniform: skips empty splits
+            // eight splits per round: all their loads are issued before the FMAs
+            for (int j0 = 0; j0 < n; j0 += 8) {
+                float x[8][4], wj[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int j = min(j0 + u, n - 1);
+                    const float wsh = __shfl_sync(0xffffffffu, w, j);
+                    wj[u] = j0 + u < n ? wsh : 0.f;
                     const float* row = mp + (s0 + j) * (kHeadDim + 1) + 4 * lane;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] += wj * row[i];
+                    for (int i = 0; i < 4; ++i) x[u][i] = row[i];
                 }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (wj[u] != 0.f) o[i] += wj[u] * x[u][i];   // skip splits of weight 0
             }
         }
         W = warp_sum(W);

@@ -4,7 +4,8 @@
 // fp32 workspace), computed per CTA = (split, sequence) over all kv heads:
 // one warp per kv head, 32-token tiles streamed into a shared-memory ring by
 // bulk (TMA) copies of whole token rows (Hk contiguous slots each) whose
-// completion is tracked by mbarriers with bounded waits.
+// completion is tracked by mbarriers with bounded waits; warps only wait for
+// data, never for each other (the last warp done with a stage refills it).
 //
 // Per tile and warp, with G query heads sharing the kv head:
 //   scores  S[t, g] = sum_d K^[t, d] Q[g, d]      A = K^ (16 tokens x 16 dims),
@@ -468,17 +469,21 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
     const int lg = a.bs_log2;
     const int seg_rows = kTile < (1 << lg) ? kTile : (1 << lg);   // rows per page segment
+    // Per stage: `full` completes when the stage's bytes have landed; `done`
+    // counts the warps finished with it.  The warp that finishes a stage last
+    // refills it, so warps never wait on each other, only on data.
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * stage_bytes);
+    int* done = reinterpret_cast<int*>(full + NST);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); done[i] = 0; }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     // Only rows of tokens < L are copied: block-table entries past the
     // sequence's last page are never read.  Skipped rows keep stale bytes and
     // are masked out of the softmax.
-    auto issue = [&](int tile) {
-        if (tile >= ntiles || warp != 0) return;
+    auto issue = [&](int tile) {            // called by all lanes of one warp
+        if (tile >= ntiles) return;
         uint8_t* dst = smem + (tile % NST) * stage_bytes;
         uint64_t* bar = &full[tile % NST];
         const int tbase = t_begin + tile * kTile;
@@ -498,7 +503,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * row_bytes), bar);
         }
     };
-    for (int i = 0; i < NST - 1; ++i) issue(i);
+    if (warp == 0)
+        for (int i = 0; i < NST; ++i) issue(i);
 
     constexpr int NH = G == 8 ? 2 : 1;        // query heads per thread (softmax state)
     float m_run[NH], l_run[NH], z_run[NH];
@@ -515,11 +521,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 
     int failed_at = -1;
     for (int it = 0; it < ntiles; ++it) {
-        // tile `it` has landed; a copy that never completes ends the split
-        // with a NaN lse instead of hanging (bounded wait)
+        // tile `it` has landed; a copy that never completes ends this warp's
+        // heads with a NaN lse instead of hanging (bounded wait)
         const bool ok_wait = mbar_wait(&full[it % NST], uint32_t((it / NST) & 1), kWaitLimit);
-        if (__syncthreads_or(!ok_wait)) { failed_at = it; break; }
-        issue(it + NST - 1);           // refills the stage of tile it-1: all warps are past it
+        if (!__all_sync(0xffffffffu, ok_wait)) { failed_at = it; break; }
         const uint8_t* st = smem + (it % NST) * stage_bytes + hoff;
         const int t0 = t_begin + it * kTile;
 
@@ -599,14 +604,27 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             p_to_b<G>(pp[rt], gid, tig, pb);
             pv_tile<VBITS, G>(st + 16 * rt * rs + a.g.off_v_data, rs, gid, tig, vmis, pb, acc);
         }
+
+        // ---- this warp is done with the stage; the last warp refills it
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&done[it % NST], 1) == nwarps - 1;
+            if (last) done[it % NST] = 0;
+            __threadfence_block();
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST);
     }
     if (failed_at >= 0) {
-        // let the copies still in flight (tiles failed_at .. failed_at + NST - 2)
-        // land, with the same bounded wait, before the CTA exits
-        for (int it = failed_at; it < min(ntiles, failed_at + NST - 1); ++it)
+        // let the copies that may still be in flight (tiles failed_at ..
+        // failed_at + NST - 1) land, with the same bounded wait, then mark
+        // this warp's heads as failed
+        for (int it = failed_at; it < min(ntiles, failed_at + NST); ++it)
             mbar_wait(&full[it % NST], uint32_t((it / NST) & 1), kWaitLimit);
-        for (int i = threadIdx.x; i < Hk * Greal; i += blockDim.x)
-            a.mid[(((long long)b * Hq + i) * S + split) * (kHeadDim + 1) + kHeadDim] = __int_as_float(0x7fc00000);
+        if (lane < Greal)
+            a.mid[(((long long)b * Hq + h * Greal + lane) * S + split) * (kHeadDim + 1) + kHeadDim] =
+                __int_as_float(0x7fc00000);
         return;
     }
 
@@ -709,7 +727,7 @@ int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const 
     // the q staging at kernel start borrows the ring: Hk * (4 or 8) heads * 512 B
     while (nst * stage < Hk * (a.G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
     a.nstages = nst;
-    const size_t smem = size_t(nst) * stage + 8 * size_t(nst);   // ring + one mbarrier per stage
+    const size_t smem = size_t(nst) * stage + 16 * size_t(nst);  // ring + mbarrier and counter per stage
     cudaError_t e = q_dtype == TQ_F16 ? launch_q<__half>(a, B, smem, st)
                                       : launch_q<__nv_bfloat16>(a, B, smem, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
