@@ -154,3 +154,40 @@ def test_planted_key_peaked_softmax(orc, preset, Hk):
     for S in (1, 8, 64):
         o, l = _gpu_decode(preset, q, pb["cache"], pb["bt"], [n], Hk, bs, pb["signs"], pb["c32"], S)
         check_decode(o, l, ref_o, ref_l, f"planted S={S}")
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_continuation_prefill_as_decode_rows(orc, preset):
+    """A continuation chunk of q_len new tokens attends causally to the cached
+    prefix by running each query row as a decode request with its own
+    sequence length (cached_len + i + 1) over one shared block-table row
+    (block_table_stride = 0), the decode-kernel path of the API page's
+    `_prefill_attention` for short continuations."""
+    rng = np.random.default_rng(900 + preset)
+    Hk, G, bs, seq_len, q_len = 8, 4, 32, 700, 13
+    cached = seq_len - q_len
+    pb = paged_problem(orc, preset, [seq_len], Hk, bs, rng)
+    dev = torch.device("cuda")
+    L = tq.tq_get_layout(preset)
+    seq_lens = np.arange(cached + 1, seq_len + 1, dtype=np.int32)          # causal per row
+    q = torch.from_numpy(rng.normal(size=(q_len, G * Hk, 128))).to(torch.float16)
+    bt_oracle = np.repeat(pb["bt"][:1], q_len, axis=0)                    # same row for every query
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], bt_oracle, seq_lens, Hk, bs,
+                                    pb["signs"], pb["c32"])
+    cache = torch.from_numpy(pb["cache"]).to(dev)
+    bt_row = torch.from_numpy(np.ascontiguousarray(pb["bt"][0])).to(dev)   # one row, stride 0
+    sl = torch.from_numpy(seq_lens).to(dev)
+    sg = torch.from_numpy(pb["signs"]).to(dev)
+    cc = torch.from_numpy(pb["c32"]).to(dev) if not L["key_fp8"] else None
+    S = tq.tq_decode_pick_splits(q_len, G * Hk, Hk, seq_len)
+    ws = torch.empty(tq.tq_decode_workspace_bytes(q_len, G * Hk, S, 128), dtype=torch.uint8, device=dev)
+    out = torch.empty((q_len, G * Hk, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((q_len, G * Hk), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = tq.tq_decode_attention(preset, 128, q_len, G * Hk, Hk, bs, tq.TQ_F16, q.to(dev).data_ptr(),
+                                cache.data_ptr(), cache.shape[0], bt_row.data_ptr(), 0, sl.data_ptr(),
+                                seq_len, 128 ** -0.5, S, sg.data_ptr(), 0 if cc is None else cc.data_ptr(),
+                                out.data_ptr(), tq.TQ_F32, lse.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+    assert rc == 0, tq.tq_status_string(rc)
+    torch.cuda.synchronize()
+    check_decode(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, f"continuation preset {preset}")
