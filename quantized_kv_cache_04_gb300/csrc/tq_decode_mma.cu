@@ -29,6 +29,7 @@
 #include "tq_internal.h"
 
 #include <cmath>
+#include <type_traits>
 
 namespace tq {
 namespace {
@@ -129,15 +130,16 @@ __device__ __forceinline__ void fence_async_shared()
 }
 
 // n little-endian 32-bit words starting at the 2-byte aligned shared address p.
-// `mis` (0 or 2, uniform per warp) is p mod 4.
-template <int N>
+// `mis` (0 or 2, uniform per warp) is p mod 4; ALIGNED promises mis == 0.
+template <int N, bool ALIGNED = false>
 __device__ __forceinline__ void lds_words(const uint8_t* p, int mis, uint32_t (&w)[N])
 {
-    const uint32_t* q = reinterpret_cast<const uint32_t*>(p - mis);
-    if (mis == 0) {
+    if (ALIGNED || mis == 0) {
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
 #pragma unroll
         for (int i = 0; i < N; ++i) w[i] = q[i];
     } else {
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(p - mis);
         uint32_t r[N + 1];
 #pragma unroll
         for (int i = 0; i <= N; ++i) r[i] = q[i];
@@ -178,19 +180,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two_bytes)
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu),
                                                      __NV_E4M3);
     return uint32_t(h.x) | (uint32_t(h.y) << 16);
-}
-
-__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b)
-{
-    __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-    return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c)
-{
-    __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
-                        *reinterpret_cast<const __half2*>(&c));
-    return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __device__ __forceinline__ float fast_exp2(float x)
@@ -316,38 +305,48 @@ __device__ __forceinline__ void p_to_b(const float (&pp)[G == 8 ? 2 : 1][2], int
 }
 
 // Value MMAs of one 16-row tile: tokens 4 tig + j of the tile, dims 16 gid + 2i (+1).
-template <int VBITS, int G>
+// A value code n (0..15) placed alone in a byte and read as FP8 E4M3 is
+// exactly n * 2^-9 (subnormal for n < 8, normal above), and that is a normal
+// fp16 number: one conversion instruction turns two such bytes into the
+// half2 of an A register.  The accumulators therefore hold 2^-9 of the value
+// sums; the epilogue scales them back by 512 (exact).
+template <int VBITS, int G, bool ALIGNED>
 __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, int tig, int vmis,
                                         const uint32_t (&pb)[2][2], float (&acc)[8][4])
 {
-    const uint32_t kMagic = 0x64006400u;       // half2(1024, 1024)
-    const uint32_t kSixteenth = 0x2C002C00u;   // half2(1/16, 1/16)
-    const uint32_t kMinus64 = 0xD400D400u;     // half2(-64, -64)
-    uint32_t vw[4][2];
+    uint32_t vw[4][2];   // per token 4 tig + j: nibble words of dims 16 gid .. 16 gid + 15
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint8_t* rv = tile_v + (4 * tig + j) * rs;
         if constexpr (VBITS == 4) {
-            lds_words<2>(rv + 8 * gid, vmis, vw[j]);
+            lds_words<2, ALIGNED>(rv + 8 * gid, vmis, vw[j]);
         } else {
             uint32_t w[3], n[4];
-            lds_words<3>(rv + 12 * (gid >> 1), vmis, w);
+            lds_words<3, ALIGNED>(rv + 12 * (gid >> 1), vmis, w);
             nibbles3(w, n);
             vw[j][0] = (gid & 1) ? n[2] : n[0];
             vw[j][1] = (gid & 1) ? n[3] : n[1];
         }
     }
+    // MMAs i and i + 1 (dims 16 gid + 2i .. 2i + 3) share one byte gather:
+    // ab = [A_i, B_i, A_i+1, B_i+1] with A, B the tokens of k = 2 tig, 2 tig + 1
+    // (cd likewise for tokens 4 tig + 2, + 3); its low nibbles give row gid
+    // (even dims), its high nibbles row gid + 8 (odd dims).
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t sel = uint32_t(i & 3) | (uint32_t((i & 3) + 4) << 8);
-        const uint32_t zab = prmt(vw[0][i >> 2], vw[1][i >> 2], sel);
-        const uint32_t zcd = prmt(vw[2][i >> 2], vw[3][i >> 2], sel);
-        const uint32_t A[4] = {hsub2_u((zab & 0x000F000Fu) | kMagic, kMagic),
-                               hfma2_u((zab & 0x00F000F0u) | kMagic, kSixteenth, kMinus64),
-                               hsub2_u((zcd & 0x000F000Fu) | kMagic, kMagic),
-                               hfma2_u((zcd & 0x00F000F0u) | kMagic, kSixteenth, kMinus64)};
-        mma16816(acc[i], A, pb[0][0], pb[0][1]);
-        if constexpr (G == 8) mma16816(acc[i], A, pb[1][0], pb[1][1]);
+    for (int i = 0; i < 8; i += 2) {
+        const uint32_t c = uint32_t(i & 3);
+        const uint32_t sel = c | ((c + 4) << 4) | ((c + 1) << 8) | ((c + 5) << 12);
+        const uint32_t ab = prmt(vw[0][i >> 2], vw[1][i >> 2], sel);
+        const uint32_t cd = prmt(vw[2][i >> 2], vw[3][i >> 2], sel);
+        uint32_t A0[4], A1[4];
+        cvt_e4m3x4(ab & 0x0F0F0F0Fu, A0[0], A1[0]);
+        cvt_e4m3x4((ab >> 4) & 0x0F0F0F0Fu, A0[1], A1[1]);
+        cvt_e4m3x4(cd & 0x0F0F0F0Fu, A0[2], A1[2]);
+        cvt_e4m3x4((cd >> 4) & 0x0F0F0F0Fu, A0[3], A1[3]);
+        mma16816(acc[i], A0, pb[0][0], pb[0][1]);
+        if constexpr (G == 8) mma16816(acc[i], A0, pb[1][0], pb[1][1]);
+        mma16816(acc[i + 1], A1, pb[0][0], pb[0][1]);
+        if constexpr (G == 8) mma16816(acc[i + 1], A1, pb[1][0], pb[1][1]);
     }
 }
 
@@ -381,17 +380,71 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         return;
     }
 
+    // ---------------- shared-memory ring of 32 token rows (all kv heads),
+    // filled by bulk (TMA) copies.  Rows of one page are contiguous in global
+    // memory: one copy per page segment when the shared row stride equals the
+    // global one, else one copy per row (issued by the 32 lanes of one warp).
+    const int row_bytes = a.row_bytes;        // global token row (Hk slots)
+    const int rs = a.smem_row;                // shared row stride: 16 mod 32 bytes
+    const int stage_bytes = kTile * rs;
+    const int NST = a.nstages;
+    const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
+    const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
+    const int lg = a.bs_log2;
+    const int seg_rows = kTile < (1 << lg) ? kTile : (1 << lg);   // rows per page segment
+    // Per stage: `full` completes when the stage's bytes have landed; `done`
+    // counts the warps finished with it.  The warp that finishes a stage last
+    // refills it, so warps never wait on each other, only on data.
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * stage_bytes);
+    int* done = reinterpret_cast<int*>(full + NST);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); done[i] = 0; }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // Only rows of tokens < L are copied: block-table entries past the
+    // sequence's last page are never read.  Skipped rows keep stale bytes and
+    // are masked out of the softmax.
+    auto issue = [&](int tile, int stage) {   // called by all lanes of one warp
+        if (tile >= ntiles) return;
+        uint8_t* dst = smem + stage * stage_bytes;
+        uint64_t* bar = &full[stage];
+        const int tbase = t_begin + tile * kTile;
+        const bool per_segment = rs == row_bytes;
+        const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile
+        const int seg_len = per_segment ? seg_rows : 1;               // rows per copy
+        const int nlive = min(nseg, (L - tbase + seg_len - 1) / seg_len);
+        if (lane == 0) {
+            fence_async_shared();             // prior generic reads of this stage before the async writes
+            mbar_expect_tx(bar, uint32_t(nlive * seg_len * row_bytes));
+        }
+        __syncwarp();
+        if (lane < nlive) {
+            const int t = tbase + lane * seg_len;
+            const long long page = bt[t >> lg];
+            const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes;
+            bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * row_bytes), bar);
+        }
+    };
+    // The q staging area (Hk x (4 or 8) heads x 512 B) sits at the end of the
+    // ring: the tiles whose stages lie wholly before it are requested first,
+    // so their latency overlaps the preparation of q.
+    const int q_base = NST * stage_bytes - Hk * G * kHeadDim * 4;
+    const int s_q = q_base / stage_bytes;
+    if (warp == 0)
+        for (int i = 0; i < s_q; ++i) issue(i, i);
+
     // ---------------- q columns: B operand of the score MMA.  Each warp
     // rotates (MSE keys) and scales its G query heads with lane l holding dims
-    // 4l..4l+3, parks them in the (still empty) ring, and every thread reads
-    // back the 32 values of its column.  The k index of k-step kk and thread
-    // tig maps to dims
+    // 4l..4l+3, parks them in the staging area, and every thread reads back
+    // the 32 values of its column.  The k index of k-step kk and thread tig
+    // maps to dims
     //   FP8 keys:   16 kk + 4 tig + j   one key word per k-step, bank-conflict
     //               free across the warp
     //   3-bit keys: 32 tig + 4 kk + j   one 32-code group (three words) per thread
     uint32_t bq[8][2], bql[8][2];
     {
-        float* sq = reinterpret_cast<float*>(smem) + h * G * kHeadDim;
+        float* sq = reinterpret_cast<float*>(smem + q_base) + h * G * kHeadDim;
         float sgn[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) sgn[i] = KMODE == 8 ? 1.f : float(a.signs[4 * lane + i]);
@@ -435,8 +488,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
                 bql[kk][1] = pack_half2(lo[2], lo[3]);
             }
         }
-        __syncthreads();            // the ring is about to receive the first tiles
+        __syncthreads();            // every warp is done with the staging area
     }
+    if (warp == 0)
+        for (int i = s_q; i < NST; ++i) issue(i, i);
 
     // ---------------- centroid byte planes for the PRMT lookup (3-bit keys):
     // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
@@ -457,55 +512,6 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
     }
 
-    // ---------------- shared-memory ring of 32 token rows (all kv heads),
-    // filled by bulk (TMA) copies.  Rows of one page are contiguous in global
-    // memory: one copy per page segment when the shared row stride equals the
-    // global one, else one copy per row (issued by the 32 lanes of warp 0).
-    const int row_bytes = a.row_bytes;        // global token row (Hk slots)
-    const int rs = a.smem_row;                // shared row stride: 16 mod 32 bytes
-    const int stage_bytes = kTile * rs;
-    const int NST = a.nstages;
-    const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
-    const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
-    const int lg = a.bs_log2;
-    const int seg_rows = kTile < (1 << lg) ? kTile : (1 << lg);   // rows per page segment
-    // Per stage: `full` completes when the stage's bytes have landed; `done`
-    // counts the warps finished with it.  The warp that finishes a stage last
-    // refills it, so warps never wait on each other, only on data.
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * stage_bytes);
-    int* done = reinterpret_cast<int*>(full + NST);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); done[i] = 0; }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    // Only rows of tokens < L are copied: block-table entries past the
-    // sequence's last page are never read.  Skipped rows keep stale bytes and
-    // are masked out of the softmax.
-    auto issue = [&](int tile) {            // called by all lanes of one warp
-        if (tile >= ntiles) return;
-        uint8_t* dst = smem + (tile % NST) * stage_bytes;
-        uint64_t* bar = &full[tile % NST];
-        const int tbase = t_begin + tile * kTile;
-        const bool per_segment = rs == row_bytes;
-        const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile
-        const int seg_len = per_segment ? seg_rows : 1;               // rows per copy
-        const int nlive = min(nseg, (L - tbase + seg_len - 1) / seg_len);
-        if (lane == 0) {
-            fence_async_shared();             // prior generic reads of this stage before the async writes
-            mbar_expect_tx(bar, uint32_t(nlive * seg_len * row_bytes));
-        }
-        __syncwarp();
-        if (lane < nlive) {
-            const int t = tbase + lane * seg_len;
-            const long long page = bt[t >> lg];
-            const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes;
-            bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * row_bytes), bar);
-        }
-    };
-    if (warp == 0)
-        for (int i = 0; i < NST; ++i) issue(i);
-
     constexpr int NH = G == 8 ? 2 : 1;        // query heads per thread (softmax state)
     float m_run[NH], l_run[NH], z_run[NH];
 #pragma unroll
@@ -519,15 +525,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     const int kmis = hoff & 2;
     const int vmis = (hoff + a.g.off_v_data) & 2;
 
-    int failed_at = -1;
-    for (int it = 0; it < ntiles; ++it) {
-        // tile `it` has landed; a copy that never completes ends this warp's
-        // heads with a NaN lse instead of hanging (bounded wait)
-        const bool ok_wait = mbar_wait(&full[it % NST], uint32_t((it / NST) & 1), kWaitLimit);
-        if (!__all_sync(0xffffffffu, ok_wait)) { failed_at = it; break; }
-        const uint8_t* st = smem + (it % NST) * stage_bytes + hoff;
-        const int t0 = t_begin + it * kTile;
-
+    // One 32-token tile in stage memory st (this warp's slot at offset 0).
+    // PARTIAL: some of its tokens lie at or past t_end and are masked.
+    auto tile = [&](const uint8_t* st, int t0, auto partial_tag) {
+        constexpr bool PARTIAL = decltype(partial_tag)::value;
         // ---- scores of both 16-row tiles
         float s[NH][2][2], vs[2][2], vz[2][2];
         bool ok[2][2];
@@ -543,8 +544,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             vz[rt][0] = lds_f16(r0 + a.g.off_v_zero);
             vs[rt][1] = lds_f16(r1 + a.g.off_v_scale);
             vz[rt][1] = lds_f16(r1 + a.g.off_v_zero);
-            ok[rt][0] = t0 + 16 * rt + tau0 < t_end;
-            ok[rt][1] = t0 + 16 * rt + tau1 < t_end;
+            ok[rt][0] = !PARTIAL || t0 + 16 * rt + tau0 < t_end;
+            ok[rt][1] = !PARTIAL || t0 + 16 * rt + tau1 < t_end;
             if constexpr (G == 4) {
                 s[0][rt][0] = (sc[0] + sc[1]) * n0;
                 s[0][rt][1] = (sc[2] + sc[3]) * n1;
@@ -556,45 +557,65 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             }
         }
 
-        // ---- one online-softmax update for the 32 tokens (log2 units)
-        float pp[2][NH][2];   // [row tile][head][row]: P' = p * v_scale
-        float alpha[NH];
+        // ---- one online-softmax update for the 32 tokens (log2 units).  The
+        // running max only moves when a head's tile max exceeds it by more
+        // than 8 (so p <= 2^8 otherwise), or when a value scale above 128
+        // could take p * v_scale out of the fp16 range of P'.  Moving it
+        // rescales the accumulators; keeping it changes no result, since
+        // o and l share the same reference.
+        float mt[NH];
+        bool need = false;
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
-            float mt = -INFINITY;
+            float m = -INFINITY;
 #pragma unroll
             for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     if (!ok[rt][r]) s[j][rt][r] = -INFINITY;
-                    mt = fmaxf(mt, s[j][rt][r]);
+                    m = fmaxf(m, s[j][rt][r]);
                 }
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-            const float mn = fmaxf(m_run[j], mt);        // finite: the tile's first token is valid
-            alpha[j] = fast_exp2(m_run[j] - mn);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            mt[j] = m;               // finite: the tile's first token is valid
+            need |= m > m_run[j] + 8.f;
+        }
+        need |= fmaxf(fmaxf(vs[0][0], vs[0][1]), fmaxf(vs[1][0], vs[1][1])) > 128.f;
+        if (__any_sync(0xffffffffu, need)) {
+            float alpha[NH];
+#pragma unroll
+            for (int j = 0; j < NH; ++j) {
+                const float mn = fmaxf(m_run[j], mt[j]);
+                alpha[j] = fast_exp2(m_run[j] - mn);
+                m_run[j] = mn;
+                l_run[j] *= alpha[j];
+                z_run[j] *= alpha[j];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if constexpr (G == 4) {
+                    acc[i][0] *= alpha[0]; acc[i][1] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][3] *= alpha[0];
+                } else {
+                    acc[i][0] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][1] *= alpha[1]; acc[i][3] *= alpha[1];
+                }
+            }
+        }
+        float pp[2][NH][2];   // [row tile][head][row]: P' = p * v_scale
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
             float lsum = 0.f, zsum = 0.f;
 #pragma unroll
             for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float p = fast_exp2(s[j][rt][r] - mn);   // 0 for masked rows
+                    const float p = fast_exp2(s[j][rt][r] - m_run[j]);   // 0 for masked rows
                     lsum += p;
                     zsum += ok[rt][r] ? p * vz[rt][r] : 0.f;
                     pp[rt][j][r] = ok[rt][r] ? p * vs[rt][r] : 0.f;
                 }
-            l_run[j] = l_run[j] * alpha[j] + lsum;
-            z_run[j] = z_run[j] * alpha[j] + zsum;
-            m_run[j] = mn;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if constexpr (G == 4) {
-                acc[i][0] *= alpha[0]; acc[i][1] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][3] *= alpha[0];
-            } else {
-                acc[i][0] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][1] *= alpha[1]; acc[i][3] *= alpha[1];
-            }
+            l_run[j] += lsum;
+            z_run[j] += zsum;
         }
 
         // ---- values
@@ -602,19 +623,34 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         for (int rt = 0; rt < 2; ++rt) {
             uint32_t pb[2][2];
             p_to_b<G>(pp[rt], gid, tig, pb);
-            pv_tile<VBITS, G>(st + 16 * rt * rs + a.g.off_v_data, rs, gid, tig, vmis, pb, acc);
+            pv_tile<VBITS, G, KMODE == 8>(st + 16 * rt * rs + a.g.off_v_data, rs, gid, tig, vmis, pb, acc);
         }
+    };
+
+    int failed_at = -1;
+    int stage = 0;               // it mod NST
+    uint32_t parity = 0;         // (it / NST) mod 2
+    for (int it = 0; it < ntiles; ++it) {
+        // tile `it` has landed; a copy that never completes ends this warp's
+        // heads with a NaN lse instead of hanging (bounded wait)
+        const bool ok_wait = mbar_wait(&full[stage], parity, kWaitLimit);
+        if (!__all_sync(0xffffffffu, ok_wait)) { failed_at = it; break; }
+        const uint8_t* st = smem + stage * stage_bytes + hoff;
+        const int t0 = t_begin + it * kTile;
+        if (t0 + kTile <= t_end) tile(st, t0, std::false_type{});
+        else                     tile(st, t0, std::true_type{});
 
         // ---- this warp is done with the stage; the last warp refills it
         __syncwarp();
         int last = 0;
         if (lane == 0) {
             __threadfence_block();
-            last = atomicAdd(&done[it % NST], 1) == nwarps - 1;
-            if (last) done[it % NST] = 0;
+            last = atomicAdd(&done[stage], 1) == nwarps - 1;
+            if (last) done[stage] = 0;
             __threadfence_block();
         }
-        if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST);
+        if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST, stage);
+        if (++stage == NST) { stage = 0; parity ^= 1u; }
     }
     if (failed_at >= 0) {
         // let the copies that may still be in flight (tiles failed_at ..
@@ -628,7 +664,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         return;
     }
 
-    // ---------------- epilogue: finish the row sums, write o_s and lse_s
+    // ---------------- epilogue: finish the row sums, write o_s and lse_s.
+    // The value accumulators hold 2^-9 of sum_t p_t v_scale_t code_t.
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
 #pragma unroll
@@ -650,8 +687,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             float e, o;
             if constexpr (G == 4) { e = acc[i][0] + acc[i][1]; o = acc[i][2] + acc[i][3]; }
             else { e = j == 0 ? acc[i][0] : acc[i][1]; o = j == 0 ? acc[i][2] : acc[i][3]; }
-            mp[d] = (e + z_run[j]) * inv;
-            mp[d + 1] = (o + z_run[j]) * inv;
+            mp[d] = (e * 512.f + z_run[j]) * inv;
+            mp[d + 1] = (o * 512.f + z_run[j]) * inv;
         }
         if (gid == 0) mp[kHeadDim] = (m_run[j] + log2f(l_run[j])) * 0.6931471805599453f;
     }
