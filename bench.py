@@ -193,7 +193,7 @@ class Problem:
         self.sl = torch.from_numpy(w.seq_lens).to(dev)
         self.max_len = int(w.seq_lens.max())
         self.S = (splits if splits else w.num_splits) or tq.tq_decode_pick_splits(
-            w.B, w.Hq, w.Hk, self.max_len)
+            self.c.preset, w.D, w.B, w.Hq, w.Hk, self.max_len)
         self.ws = self.c.workspace(w.B, w.Hq, self.S)
         self.out = torch.empty((w.B, w.Hq, w.D), dtype=self.q.dtype, device=dev)
         self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)

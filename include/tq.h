@@ -134,10 +134,19 @@ int tq_store(int preset, int head_dim, int num_tokens, int num_kv_heads, int blo
              void* stream);
 
 /* Split count the library uses when tq_decode_attention gets num_splits = 0,
- * from host-known sizes only (no device read).  max_seq_len is an upper
- * bound on seq_lens.  Returns a value in [1, TQ_MAX_SPLITS]. */
+ * from host-known sizes (no device memory is read; the current device's SM
+ * count and the stage-1 kernel's occupancy are queried, and cached).  It
+ * minimises the stage-1 critical path: the waves of (split, sequence, head
+ * group) CTAs over the resident CTA slots, times the 32-token tiles of one
+ * split plus a fixed start-up cost; splits are at least 128 tokens long.
+ * max_seq_len is an upper bound on seq_lens.  Returns a value in
+ * [1, TQ_MAX_SPLITS] (1 for non-positive sizes), or TQ_ERR_UNSUPPORTED /
+ * TQ_ERR_INVALID_ARG for an unknown preset or head_dim, or a head count that
+ * is not a multiple of num_kv_heads.  Without a device it assumes two CTAs
+ * per SM of a 152-SM GB300. */
 #define TQ_MAX_SPLITS 256
-int tq_decode_pick_splits(int batch, int num_q_heads, int num_kv_heads, int max_seq_len);
+int tq_decode_pick_splits(int preset, int head_dim, int batch, int num_q_heads, int num_kv_heads,
+                          int max_seq_len);
 
 /* Bytes of caller-owned workspace tq_decode_attention needs: the stage-1
  * partials mid_o fp32 [batch][num_q_heads][num_splits][head_dim + 1] (column

@@ -63,7 +63,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.tq_make_signs.argtypes = [_c_int, ctypes.c_uint64, _c_vp]
     L.tq_store.argtypes = ([_c_int] * 6 + [_c_vp, _c_vp, _c_ll, _c_ll, _c_vp, _c_vp, _c_ll]
                            + [_c_vp] * 4)
-    L.tq_decode_pick_splits.argtypes = [_c_int] * 4
+    L.tq_decode_pick_splits.argtypes = [_c_int] * 6
     L.tq_decode_workspace_bytes.argtypes = [_c_int] * 4
     L.tq_decode_workspace_bytes.restype = _c_sz
     L.tq_decode_attention.argtypes = ([_c_int] * 7 + [_c_vp, _c_vp, _c_ll, _c_vp, _c_int, _c_vp,
@@ -115,9 +115,13 @@ def tq_make_signs(head_dim: int, seed: int = 42):
     return s
 
 
-def tq_decode_pick_splits(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int) -> int:
-    return load().tq_decode_pick_splits(int(batch), int(num_q_heads), int(num_kv_heads),
-                                        int(max_seq_len))
+def tq_decode_pick_splits(preset: int, head_dim: int, batch: int, num_q_heads: int,
+                          num_kv_heads: int, max_seq_len: int) -> int:
+    s = load().tq_decode_pick_splits(int(preset), int(head_dim), int(batch), int(num_q_heads),
+                                     int(num_kv_heads), int(max_seq_len))
+    if s < 0:
+        raise TQError("tq_decode_pick_splits", s)
+    return s
 
 
 def tq_decode_kernel_kind(preset: int, head_dim: int, num_q_heads: int, num_kv_heads: int) -> int:

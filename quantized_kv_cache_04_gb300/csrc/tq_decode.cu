@@ -17,20 +17,10 @@
 #include "tq_internal.h"
 
 #include <cmath>
+#include <mutex>
+#include <vector>
 
 namespace tq {
-
-int pick_splits(int batch, int num_kv_heads, int max_seq_len)
-{
-    if (batch <= 0 || num_kv_heads <= 0 || max_seq_len <= 0) return 1;
-    // about four CTAs of (split, sequence) per SM, each split >= 256 tokens
-    long long s = (4LL * kNumSMs + batch - 1) / batch;
-    const long long by_len = (max_seq_len + 255) / 256;
-    if (s > by_len) s = by_len;
-    if (s < 1) s = 1;
-    if (s > TQ_MAX_SPLITS) s = TQ_MAX_SPLITS;
-    return int(s);
-}
 
 namespace {
 
@@ -225,43 +215,52 @@ constexpr int kStage2Warps = 4;
 template <typename TO>
 __global__ void __launch_bounds__(32 * kStage2Warps) stage2_kernel(DecodeArgs a)
 {
+    // launched as a programmatic dependent of stage 1: wait until its
+    // partials are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const long long bh = (long long)blockIdx.x * kStage2Warps + (threadIdx.x >> 5);   // b * Hq + hq
     if (bh >= (long long)a.B * a.Hq) return;
     const int S = a.num_splits;
     const float* mp = a.mid + bh * S * (kHeadDim + 1);
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, mp[s * (kHeadDim + 1) + kHeadDim]);
-    M = warp_max(M);
+    // One pass over the splits in rounds of kRound: every load of a round is
+    // issued before any arithmetic, and the running max M moves by rescaling
+    // (the log-sum-exp merge of the split partials).  A NaN lse (a split
+    // that gave up waiting for its data) makes the row NaN.
+    constexpr int kRound = 16;
+    float M = -INFINITY, W = 0.f;
     float o[4] = {0.f, 0.f, 0.f, 0.f};
-    float W = 0.f;
-    if (M != -INFINITY) {
-        for (int s0 = 0; s0 < S; s0 += 32) {
-            const int s = s0 + lane;
-            const float ls = s < S ? mp[s * (kHeadDim + 1) + kHeadDim] : -INFINITY;
-            const float w = ls == -INFINITY ? 0.f : expf(ls - M);
+    for (int s0 = 0; s0 < S; s0 += kRound) {
+        float ls[kRound], x[kRound][4];
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+            const float* row = mp + min(s0 + u, S - 1) * (kHeadDim + 1);
+            ls[u] = s0 + u < S ? row[kHeadDim] : -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[u][i] = row[4 * lane + i];
+        }
+        float mc = M;
+        bool nan = false;
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) { mc = fmaxf(mc, ls[u]); nan |= ls[u] != ls[u]; }
+        if (nan) { M = W = __int_as_float(0x7fc00000); break; }
+        if (mc == -INFINITY) continue;            // only empty splits so far
+        const float sc = expf(M - mc);            // 0 while M = -inf
+        W *= sc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] *= sc;
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+            const float w = expf(ls[u] - mc);     // 0 for empty and padding splits
             W += w;
-            const int n = min(32, S - s0);
-            // eight splits per round: all their loads are issued before the FMAs
-            for (int j0 = 0; j0 < n; j0 += 8) {
-                float x[8][4], wj[8];
+            if (w != 0.f) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int j = min(j0 + u, n - 1);
-                    const float wsh = __shfl_sync(0xffffffffu, w, j);
-                    wj[u] = j0 + u < n ? wsh : 0.f;
-                    const float* row = mp + (s0 + j) * (kHeadDim + 1) + 4 * lane;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) x[u][i] = row[i];
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (wj[u] != 0.f) o[i] += wj[u] * x[u][i];   // skip splits of weight 0
+                for (int i = 0; i < 4; ++i) o[i] += w * x[u][i];
             }
         }
-        W = warp_sum(W);
+        M = mc;
+    }
+    if (M != -INFINITY) {
         const float inv = 1.f / W;
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] *= inv;
@@ -270,6 +269,23 @@ __global__ void __launch_bounds__(32 * kStage2Warps) stage2_kernel(DecodeArgs a)
 #pragma unroll
     for (int i = 0; i < 4; ++i) out[i] = from_f32<TO>(o[i]);
     if (lane == 0 && a.lse) a.lse[bh] = M == -INFINITY ? -INFINITY : M + logf(W);
+}
+
+template <typename TO>
+cudaError_t launch_stage2(const DecodeArgs& a, cudaStream_t st)
+{
+    const unsigned rows = unsigned(a.B) * a.Hq;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + kStage2Warps - 1) / kStage2Warps);
+    cfg.blockDim = dim3(32 * kStage2Warps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stage2_kernel<TO>, a);
 }
 
 template <typename TQ, bool FP8, int KB, int VB>
@@ -296,7 +312,91 @@ cudaError_t launch_stage1(int preset, const DecodeArgs& a, cudaStream_t st)
     return cudaErrorInvalidValue;
 }
 
+template <bool FP8, int KB, int VB>
+int v1_slots(int G, int num_sms)
+{
+    int per_sm = 0;
+    cudaError_t e;
+    if (G <= 1) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stage1_kernel<__nv_bfloat16, FP8, KB, VB, 1>, kWarps * 32, 0);
+    else if (G <= 2) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stage1_kernel<__nv_bfloat16, FP8, KB, VB, 2>, kWarps * 32, 0);
+    else if (G <= 4) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stage1_kernel<__nv_bfloat16, FP8, KB, VB, 4>, kWarps * 32, 0);
+    else if (G <= 8) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stage1_kernel<__nv_bfloat16, FP8, KB, VB, 8>, kWarps * 32, 0);
+    else e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stage1_kernel<__nv_bfloat16, FP8, KB, VB, 16>, kWarps * 32, 0);
+    return e == cudaSuccess ? per_sm * num_sms : 0;
+}
+
+// (CTAs per split, resident CTA slots) of the stage-1 kernel for a shape,
+// cached per device.
+void stage1_shape(const tq_layout& L, int Hk, int G, int* cps, int* slots)
+{
+    struct Entry { int dev, kf8, kb, vb, hk, g, cps, slots; };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = -1, num_sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();        // no device: clear the error, use the defaults below
+        dev = -1;
+        num_sms = 0;
+    }
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache)
+            if (e.dev == dev && e.kf8 == L.key_fp8 && e.kb == L.key_bits && e.vb == L.value_bits &&
+                e.hk == Hk && e.g == G) {
+                *cps = e.cps;
+                *slots = e.slots;
+                return;
+            }
+    }
+    int c = Hk, n = 0;
+    if (mma_stage1_supported(L, Hk, G)) {
+        mma_stage1_shape(L, Hk, G, num_sms, &c, &n);
+    } else if (num_sms > 0) {
+        c = Hk;                    // grid (splits, kv heads, batch)
+        if (L.key_fp8) n = v1_slots<true, 4, 4>(G, num_sms);
+        else if (L.key_bits == 4) n = v1_slots<false, 4, 4>(G, num_sms);
+        else if (L.value_bits == 4) n = v1_slots<false, 3, 4>(G, num_sms);
+        else n = v1_slots<false, 3, 3>(G, num_sms);
+    }
+    if (n <= 0) {
+        cudaGetLastError();
+        n = 2 * kNumSMs;           // no device to ask: two CTAs per SM of a GB300
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 256) cache.push_back({dev, L.key_fp8, L.key_bits, L.value_bits, Hk, G, c, n});
+    *cps = c;
+    *slots = n;
+}
+
 }  // namespace
+
+int pick_splits(const tq_layout& L, int batch, int num_q_heads, int num_kv_heads, int max_seq_len)
+{
+    if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_seq_len <= 0) return 1;
+    int cps = 1, slots = 1;
+    stage1_shape(L, num_kv_heads, num_q_heads / num_kv_heads, &cps, &slots);
+    // Critical path of stage 1 in 32-token tiles: the CTAs of all splits run
+    // in ceil(CTAs / slots) waves, each as long as one split's tiles plus a
+    // fixed start-up (q preparation, first copy latency, epilogue) worth about
+    // kStartTiles tiles.  Splits shorter than 128 tokens are not used.
+    constexpr double kStartTiles = 3.0;
+    long long max_s = (max_seq_len + 127) / 128;
+    if (max_s > TQ_MAX_SPLITS) max_s = TQ_MAX_SPLITS;
+    if (max_s < 1) max_s = 1;
+    int best = 1;
+    double best_cost = 0.0;
+    for (long long s = 1; s <= max_s; ++s) {
+        const long long ctas = (long long)batch * s * cps;
+        const long long waves = (ctas + slots - 1) / slots;
+        const long long chunk = (max_seq_len + s - 1) / s;
+        const long long tiles = (chunk + 31) / 32;
+        const double cost = double(waves) * (double(tiles) + kStartTiles);
+        if (s == 1 || cost < best_cost * (1.0 - 1e-9)) { best = int(s); best_cost = cost; }
+    }
+    return best;
+}
+
 }  // namespace tq
 
 extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,
@@ -326,7 +426,7 @@ extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_
         return TQ_ERR_INVALID_ARG;
     if (!L.key_fp8 && (!signs || !centroids)) return TQ_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) & 15) return TQ_ERR_INVALID_ARG;
-    const int S = num_splits ? num_splits : pick_splits(batch, num_kv_heads, max_seq_len);
+    const int S = num_splits ? num_splits : pick_splits(L, batch, num_q_heads, num_kv_heads, max_seq_len);
     if (workspace_bytes < tq_decode_workspace_bytes(batch, num_q_heads, S, head_dim))
         return TQ_ERR_WORKSPACE;
 
@@ -362,12 +462,10 @@ extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_
                                           : launch_stage1<__nv_bfloat16>(preset, a, st);
         if (e != cudaSuccess) return TQ_ERR_CUDA;
     }
-    const unsigned rows = unsigned(batch) * num_q_heads;
-    const unsigned grid2 = (rows + kStage2Warps - 1) / kStage2Warps;
-    if (out_dtype == TQ_F32) stage2_kernel<float><<<grid2, 32 * kStage2Warps, 0, st>>>(a);
-    else if (out_dtype == TQ_F16) stage2_kernel<__half><<<grid2, 32 * kStage2Warps, 0, st>>>(a);
-    else stage2_kernel<__nv_bfloat16><<<grid2, 32 * kStage2Warps, 0, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    const cudaError_t e2 = out_dtype == TQ_F32 ? launch_stage2<float>(a, st)
+                           : out_dtype == TQ_F16 ? launch_stage2<__half>(a, st)
+                                                 : launch_stage2<__nv_bfloat16>(a, st);
+    return e2 == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 extern "C" int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, int num_kv_heads)

@@ -46,8 +46,10 @@ struct MmaArgs {
     const float* centroids;
     float* mid;              // (B, Hq, S, D+1)
     int Hq, Hk, G, bs, bs_log2;
-    int row_bytes;           // Hk * slot
-    int smem_row;            // row_bytes padded to 16 mod 32 bytes
+    int row_bytes;           // global token row: Hk * slot
+    int hpc;                 // kv heads per CTA (Hk, or 4 for FP8 keys)
+    int copy_bytes;          // hpc * slot: the part of a token row one CTA copies
+    int smem_row;            // copy_bytes padded to 16 mod 32 bytes
     int nstages;
     SlotGeom g;
 };
@@ -361,8 +363,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     const int split = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const int h = warp;
-    const int S = a.num_splits, Hk = a.Hk, Hq = a.Hq, Greal = a.G;
+    const int h0 = blockIdx.z * a.hpc;        // first kv head of this CTA
+    const int h = h0 + warp;                   // this warp's kv head
+    const int S = a.num_splits, Hq = a.Hq, Greal = a.G;
+    const int Hc = a.hpc;
     const int nwarps = blockDim.x >> 5;
 
     const int L = a.seq_lens[b];
@@ -372,19 +376,21 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     const int t_end = min(L, t_begin + chunk);
 
     if (t_begin >= t_end) {      // empty split: lse = -inf and a zero partial
-        for (int i = threadIdx.x; i < Hk * Greal * (kHeadDim + 1); i += blockDim.x) {
-            const int hq = i / (kHeadDim + 1), d = i % (kHeadDim + 1);
+        for (int i = threadIdx.x; i < Hc * Greal * (kHeadDim + 1); i += blockDim.x) {
+            const int hq = h0 * Greal + i / (kHeadDim + 1), d = i % (kHeadDim + 1);
             float* m = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
             m[d] = d == kHeadDim ? -INFINITY : 0.f;
         }
         return;
     }
 
-    // ---------------- shared-memory ring of 32 token rows (all kv heads),
-    // filled by bulk (TMA) copies.  Rows of one page are contiguous in global
-    // memory: one copy per page segment when the shared row stride equals the
-    // global one, else one copy per row (issued by the 32 lanes of one warp).
+    // ---------------- shared-memory ring of 32 token rows (the CTA's kv
+    // heads), filled by bulk (TMA) copies.  Rows of one page are contiguous in
+    // global memory: one copy per page segment when the CTA takes whole rows
+    // and the shared row stride equals the global one, else one copy per row
+    // (issued by the 32 lanes of one warp).
     const int row_bytes = a.row_bytes;        // global token row (Hk slots)
+    const int cb = a.copy_bytes;              // bytes of it this CTA copies
     const int rs = a.smem_row;                // shared row stride: 16 mod 32 bytes
     const int stage_bytes = kTile * rs;
     const int NST = a.nstages;
@@ -410,26 +416,27 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         uint8_t* dst = smem + stage * stage_bytes;
         uint64_t* bar = &full[stage];
         const int tbase = t_begin + tile * kTile;
-        const bool per_segment = rs == row_bytes;
+        const bool per_segment = rs == row_bytes && cb == row_bytes;
         const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile
         const int seg_len = per_segment ? seg_rows : 1;               // rows per copy
         const int nlive = min(nseg, (L - tbase + seg_len - 1) / seg_len);
         if (lane == 0) {
             fence_async_shared();             // prior generic reads of this stage before the async writes
-            mbar_expect_tx(bar, uint32_t(nlive * seg_len * row_bytes));
+            mbar_expect_tx(bar, uint32_t(nlive * seg_len * cb));
         }
         __syncwarp();
         if (lane < nlive) {
             const int t = tbase + lane * seg_len;
             const long long page = bt[t >> lg];
-            const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes;
-            bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * row_bytes), bar);
+            const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes +
+                                 h0 * a.g.slot;
+            bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * cb), bar);
         }
     };
-    // The q staging area (Hk x (4 or 8) heads x 512 B) sits at the end of the
+    // The q staging area (hpc x (4 or 8) heads x 512 B) sits at the end of the
     // ring: the tiles whose stages lie wholly before it are requested first,
     // so their latency overlaps the preparation of q.
-    const int q_base = NST * stage_bytes - Hk * G * kHeadDim * 4;
+    const int q_base = NST * stage_bytes - Hc * G * kHeadDim * 4;
     const int s_q = q_base / stage_bytes;
     if (warp == 0)
         for (int i = 0; i < s_q; ++i) issue(i, i);
@@ -444,7 +451,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     //   3-bit keys: 32 tig + 4 kk + j   one 32-code group (three words) per thread
     uint32_t bq[8][2], bql[8][2];
     {
-        float* sq = reinterpret_cast<float*>(smem + q_base) + h * G * kHeadDim;
+        float* sq = reinterpret_cast<float*>(smem + q_base) + warp * G * kHeadDim;
         float sgn[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) sgn[i] = KMODE == 8 ? 1.f : float(a.signs[4 * lane + i]);
@@ -521,7 +528,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
     const int tau0 = qk_token(gid), tau1 = qk_token(gid + 8);
-    const int hoff = h * a.g.slot;
+    const int hoff = warp * a.g.slot;          // this warp's slot in a shared row
     const int kmis = hoff & 2;
     const int vmis = (hoff + a.g.off_v_data) & 2;
 
@@ -652,6 +659,9 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST, stage);
         if (++stage == NST) { stage = 0; parity ^= 1u; }
     }
+    // stage 2 (a programmatic dependent launch) may start its launch now; it
+    // waits for this grid's completion before it reads the partials
+    asm volatile("griddepcontrol.launch_dependents;");
     if (failed_at >= 0) {
         // let the copies that may still be in flight (tiles failed_at ..
         // failed_at + NST - 1) land, with the same bounded wait, then mark
@@ -700,8 +710,8 @@ cudaError_t launch_t(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
     auto k = stage1_mma_kernel<TQ, KMODE, VBITS, G>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(a.num_splits, B);
-    k<<<grid, 32 * a.Hk, smem, st>>>(a);
+    dim3 grid(a.num_splits, B, a.Hk / a.hpc);
+    k<<<grid, 32 * a.hpc, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -720,15 +730,77 @@ cudaError_t launch_q(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
     return launch_g<TQ, 3, 3>(a, B, smem, st);
 }
 
+// Launch geometry shared by the launcher and the occupancy query.
+struct MmaGeom {
+    int hpc, copy_bytes, smem_row, nstages;
+    size_t smem;
+};
+
+MmaGeom mma_geom(const tq_layout& L, int Hk, int G)
+{
+    MmaGeom m;
+    // FP8-key rows split into CTAs of 4 kv heads (4 x 196 B is a whole number
+    // of 16-byte copy units): half-size CTAs, four per SM, each waiting on
+    // only 4 warps before a stage is refilled
+    m.hpc = (L.key_fp8 && Hk % 4 == 0 && Hk > 4 && (4 * L.slot_size_aligned) % 16 == 0) ? 4 : Hk;
+    m.copy_bytes = m.hpc * L.slot_size_aligned;
+    // a shared row stride of 16 mod 32 bytes (4 mod 8 words) puts the rows a
+    // warp reads in the same instruction on distinct bank quads
+    m.smem_row = (m.copy_bytes % 32 == 0) ? m.copy_bytes + 16 : m.copy_bytes;
+    const int stage = kTile * m.smem_row;
+    // ring budget: two CTAs of Hk warps, or four CTAs of 4 warps, per SM
+    int nst = (m.hpc < Hk ? 56 * 1024 : 100 * 1024) / stage;
+    nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
+    // the q staging at kernel start borrows the ring: hpc * (4 or 8) heads * 512 B
+    while (nst * stage < m.hpc * (G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
+    m.nstages = nst;
+    m.smem = size_t(nst) * stage + 16 * size_t(nst);   // ring + mbarrier and counter per stage
+    return m;
+}
+
+template <int KMODE, int VBITS, int G>
+int slots_t(const MmaGeom& m, int num_sms)
+{
+    auto k = stage1_mma_kernel<__nv_bfloat16, KMODE, VBITS, G>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(m.smem)) != cudaSuccess)
+        return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 32 * m.hpc, m.smem) != cudaSuccess)
+        return 0;
+    return per_sm * num_sms;
+}
+
 }  // namespace
 
 bool mma_stage1_supported(const tq_layout& L, int num_kv_heads, int group)
 {
     const bool keys_ok = (L.key_fp8 && L.value_bits == 4) || (!L.key_fp8 && L.key_bits == 3);
     const bool vals_ok = L.value_bits == 3 || L.value_bits == 4;
-    const int row = num_kv_heads * L.slot_size_aligned;
-    return keys_ok && vals_ok && num_kv_heads >= 1 && num_kv_heads <= 16 && group >= 1 &&
-           group <= 8 && row % 16 == 0 && 2 * kTile * (row + 16) <= 110 * 1024;
+    if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > 8) return false;
+    const MmaGeom m = mma_geom(L, num_kv_heads, group);
+    const int row = m.copy_bytes;
+    return m.hpc <= 16 && row % 16 == 0 && 2 * kTile * (row + 16) <= 110 * 1024;
+}
+
+void mma_stage1_shape(const tq_layout& L, int num_kv_heads, int group, int num_sms, int* ctas_per_split,
+                      int* slots)
+{
+    const MmaGeom m = mma_geom(L, num_kv_heads, group);
+    *ctas_per_split = num_kv_heads / m.hpc;
+    int n = 0;
+    if (num_sms > 0) {
+        if (L.key_fp8) n = group <= 4 ? slots_t<8, 4, 4>(m, num_sms) : slots_t<8, 4, 8>(m, num_sms);
+        else if (L.value_bits == 4) n = group <= 4 ? slots_t<3, 4, 4>(m, num_sms) : slots_t<3, 4, 8>(m, num_sms);
+        else n = group <= 4 ? slots_t<3, 3, 4>(m, num_sms) : slots_t<3, 3, 8>(m, num_sms);
+    }
+    if (n <= 0) {
+        // no device to ask: a GB300 SM's 228 KB of shared memory (1 KB kept
+        // per CTA) and 64K registers at 128 per thread
+        const int by_smem = int((228 * 1024) / (m.smem + 1024));
+        const int by_regs = 65536 / (128 * 32 * m.hpc);
+        n = (by_smem < by_regs ? by_smem : by_regs) * kNumSMs;
+    }
+    *slots = n;
 }
 
 int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const uint8_t* kv_cache,
@@ -754,19 +826,14 @@ int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const 
     a.bs = bs;
     a.bs_log2 = bs == 16 ? 4 : bs == 32 ? 5 : bs == 64 ? 6 : 7;
     a.row_bytes = Hk * L.slot_size_aligned;
-    // a shared row stride of 16 mod 32 bytes (4 mod 8 words) puts the rows a
-    // warp reads in the same instruction on distinct bank quads
-    a.smem_row = (a.row_bytes % 32 == 0) ? a.row_bytes + 16 : a.row_bytes;
+    const MmaGeom m = mma_geom(L, Hk, a.G);
+    a.hpc = m.hpc;
+    a.copy_bytes = m.copy_bytes;
+    a.smem_row = m.smem_row;
+    a.nstages = m.nstages;
     a.g = geom_of(L);
-    const int stage = kTile * a.smem_row;
-    int nst = (100 * 1024) / stage;          // ~100 KB of ring: two CTAs per SM
-    nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
-    // the q staging at kernel start borrows the ring: Hk * (4 or 8) heads * 512 B
-    while (nst * stage < Hk * (a.G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
-    a.nstages = nst;
-    const size_t smem = size_t(nst) * stage + 16 * size_t(nst);  // ring + mbarrier and counter per stage
-    cudaError_t e = q_dtype == TQ_F16 ? launch_q<__half>(a, B, smem, st)
-                                      : launch_q<__nv_bfloat16>(a, B, smem, st);
+    cudaError_t e = q_dtype == TQ_F16 ? launch_q<__half>(a, B, m.smem, st)
+                                      : launch_q<__nv_bfloat16>(a, B, m.smem, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

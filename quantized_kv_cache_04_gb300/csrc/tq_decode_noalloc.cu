@@ -54,7 +54,9 @@ extern "C" int tq_decode_attention_noalloc(int preset, int head_dim, int batch, 
     if (batch > 0 && num_q_heads > 0 && head_dim > 0 && num_splits >= 0) {
         const size_t per_split = tq_decode_workspace_bytes(batch, num_q_heads, 1, head_dim);
         if (splits == 0) {
-            splits = tq_decode_pick_splits(batch, num_q_heads, num_kv_heads, max_seq_len);
+            splits = tq_decode_pick_splits(preset, head_dim, batch, num_q_heads, num_kv_heads,
+                                           max_seq_len);
+            if (splits < 0) return splits;
             const size_t fit = per_split ? TQ_NOALLOC_SCRATCH_BYTES / per_split : 0;
             if ((size_t)splits > fit) splits = (int)fit;
         }

@@ -114,10 +114,14 @@ extern "C" size_t tq_decode_workspace_bytes(int batch, int num_q_heads, int num_
     return (size_t)batch * num_q_heads * num_splits * (head_dim + 1) * sizeof(float);
 }
 
-extern "C" int tq_decode_pick_splits(int batch, int num_q_heads, int num_kv_heads, int max_seq_len)
+extern "C" int tq_decode_pick_splits(int preset, int head_dim, int batch, int num_q_heads,
+                                     int num_kv_heads, int max_seq_len)
 {
-    (void)num_q_heads;
-    return tq::pick_splits(batch, num_kv_heads, max_seq_len);
+    tq_layout L;
+    const int rc = tq::fill_layout(preset, head_dim, &L);
+    if (rc) return rc;
+    if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return TQ_ERR_INVALID_ARG;
+    return tq::pick_splits(L, batch, num_q_heads, num_kv_heads, max_seq_len);
 }
 
 extern "C" const char* tq_status_string(int status)

@@ -14,7 +14,9 @@ constexpr int kMaxGroup = 16;     // query heads per kv head served by decode
 constexpr int kNumSMs = 152;      // GB300
 
 int fill_layout(int preset, int head_dim, tq_layout* L);
-int pick_splits(int batch, int num_kv_heads, int max_seq_len);
+// Split count for num_splits = 0 (tq_decode.cu): the one that minimises the
+// stage-1 critical path over the resident CTA slots of the kernel that runs.
+int pick_splits(const tq_layout& L, int batch, int num_q_heads, int num_kv_heads, int max_seq_len);
 
 inline bool block_size_ok(int bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128; }
 inline bool in_dtype_ok(int dt) { return dt == TQ_F16 || dt == TQ_BF16; }
@@ -45,6 +47,10 @@ inline SlotGeom geom_of(const tq_layout& L)
 
 // Tensor-core stage 1 (tq_decode_mma.cu): which shapes it serves, and its launcher.
 bool mma_stage1_supported(const tq_layout& L, int num_kv_heads, int group);
+// CTAs one split of one sequence launches, and resident CTA slots on num_sms
+// SMs (0 when the occupancy query fails, e.g. without a device).
+void mma_stage1_shape(const tq_layout& L, int num_kv_heads, int group, int num_sms, int* ctas_per_split,
+                      int* slots);
 int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const uint8_t* kv_cache,
                       const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,

@@ -23,7 +23,7 @@ def _gpu_decode(preset, q, cache_np, bt, seq_lens, Hk, bs, signs, c32, num_split
     sg = torch.from_numpy(signs).to(dev)
     cc = torch.from_numpy(c32).to(dev) if not L["key_fp8"] else None
     maxlen = int(max(seq_lens)) if len(seq_lens) else 0
-    S = num_splits or tq.tq_decode_pick_splits(B, Hq, Hk, maxlen)
+    S = num_splits or tq.tq_decode_pick_splits(preset, D, B, Hq, Hk, maxlen)
     ws = torch.empty(max(16, tq.tq_decode_workspace_bytes(B, Hq, S, D)), dtype=torch.uint8,
                      device=dev)
     out = torch.empty((B, Hq, D), dtype=out_dtype, device=dev)
@@ -52,12 +52,14 @@ CASES = [  # (G, Hk, bs, seq_lens, splits): CUDA-core and tensor-core stage 1 sh
 
 
 def _expected_kind(preset, G, Hk):
-    """Tensor-core stage 1 serves FP8 / 3-bit keys, G <= 8, Hk <= 16 and
-    token rows that are whole 16-byte units and fit a two-stage ring of 32
-    rows in ~110 KB of shared memory."""
+    """Tensor-core stage 1 serves FP8 / 3-bit keys and G <= 8.  A CTA takes
+    the token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above 4) or of
+    all Hk <= 16 heads; that part of a row must be whole 16-byte units and a
+    two-stage ring of 32 such rows must fit in ~110 KB of shared memory."""
     slot = [196, 134, 118, 102][preset]
-    row = Hk * slot
-    return int(preset != 1 and G <= 8 and Hk <= 16 and row % 16 == 0
+    hpc = 4 if (preset == 0 and Hk % 4 == 0 and Hk > 4) else Hk
+    row = hpc * slot
+    return int(preset != 1 and G <= 8 and hpc <= 16 and row % 16 == 0
                and 2 * 32 * (row + 16) <= 110 * 1024)
 
 
@@ -179,7 +181,7 @@ def test_continuation_prefill_as_decode_rows(orc, preset):
     sl = torch.from_numpy(seq_lens).to(dev)
     sg = torch.from_numpy(pb["signs"]).to(dev)
     cc = torch.from_numpy(pb["c32"]).to(dev) if not L["key_fp8"] else None
-    S = tq.tq_decode_pick_splits(q_len, G * Hk, Hk, seq_len)
+    S = tq.tq_decode_pick_splits(preset, 128, q_len, G * Hk, Hk, seq_len)
     ws = torch.empty(tq.tq_decode_workspace_bytes(q_len, G * Hk, S, 128), dtype=torch.uint8, device=dev)
     out = torch.empty((q_len, G * Hk, 128), dtype=torch.float32, device=dev)
     lse = torch.empty((q_len, G * Hk), dtype=torch.float32, device=dev)

@@ -64,9 +64,15 @@ def test_signs_match_oracle(orc):
 def test_sizing():
     assert tq.tq_decode_workspace_bytes(32, 32, 16, 128) == 32 * 32 * 16 * 129 * 4
     assert tq.tq_decode_workspace_bytes(0, 32, 16, 128) == 0
-    for B, Hk, L in [(1, 2, 512), (32, 8, 8192), (4, 8, 262144), (64, 8, 32768), (1, 1, 1)]:
-        s = tq.tq_decode_pick_splits(B, Hk * 4, Hk, L)
-        assert 1 <= s <= _lib.TQ_MAX_SPLITS
+    for preset in range(4):
+        for B, Hk, L in [(1, 2, 512), (32, 8, 8192), (4, 8, 262144), (64, 8, 32768), (1, 1, 1),
+                         (0, 8, 100), (3, 8, 0)]:
+            s = tq.tq_decode_pick_splits(preset, 128, B, Hk * 4, Hk, L)
+            assert 1 <= s <= _lib.TQ_MAX_SPLITS
+            assert s <= max(1, (L + 127) // 128)          # splits of at least 128 tokens
+    for bad in [(7, 128, 1, 8, 2, 64), (0, 128, 1, 6, 4, 64), (0, 128, 1, 8, 0, 64)]:
+        with pytest.raises(tq.TQError):
+            tq.tq_decode_pick_splits(*bad)
     assert tq.tq_status_string(0) == "ok"
     assert "workspace" in tq.tq_status_string(-3)
 

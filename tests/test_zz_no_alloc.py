@@ -55,7 +55,7 @@ def _args(p, num_splits, out, lse):
 
 
 def _with_workspace(p, num_splits):
-    S = num_splits or tq.tq_decode_pick_splits(p["B"], p["Hq"], p["Hk"], p["ctx"])
+    S = num_splits or tq.tq_decode_pick_splits(p["preset"], 128, p["B"], p["Hq"], p["Hk"], p["ctx"])
     ws = torch.empty(tq.tq_decode_workspace_bytes(p["B"], p["Hq"], S, 128), dtype=torch.uint8,
                      device="cuda")
     out = torch.empty((p["B"], p["Hq"], 128), dtype=torch.float32, device="cuda")
