@@ -200,12 +200,34 @@ __device__ __forceinline__ void cvt_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& h
         : "r"(w));
 }
 
+// 16-entry centroid lookup (4-bit keys) of the four codes in the low 16 bits
+// of s (code j in nibble j).  PRMT indexes 8 bytes, so each byte plane has a
+// table for codes 0-7 (T[2p]) and one for codes 8-15 (T[2p + 1]); both are
+// read with the low 3 bits of every code and a third PRMT keeps, per byte,
+// the one that bit 3 names.  Planes: 0/1 = low/high byte of fp16(c), 2/3 =
+// low/high byte of the fp16 residual.  h0/h1 (l0/l1): the hi (lo) halves of
+// codes 0,1 and 2,3 as half2.
+__device__ __forceinline__ void lut16(const uint32_t (&T)[8][2], uint32_t s, uint32_t& h0, uint32_t& h1,
+                                      uint32_t& l0, uint32_t& l1)
+{
+    const uint32_t s7 = s & 0x7777u;
+    const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;   // byte j from the second word if bit 3 set
+    uint32_t x[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        x[p] = prmt(prmt(T[2 * p][0], T[2 * p][1], s7), prmt(T[2 * p + 1][0], T[2 * p + 1][1], s7), pick);
+    h0 = prmt(x[0], x[1], 0x5140u);
+    h1 = prmt(x[0], x[1], 0x7362u);
+    l0 = prmt(x[2], x[3], 0x5140u);
+    l1 = prmt(x[2], x[3], 0x7362u);
+}
+
 // Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1: row gid+8).
 // Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
-template <int KMODE, int G>
+template <int KMODE, int G, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
-                                        const uint32_t (&T)[4][2], float (&out)[4], float (&outl)[4])
+                                        const uint32_t (&T)[NT][2], float (&out)[4], float (&outl)[4])
 {
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float scl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -221,31 +243,42 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
             if constexpr (G == 8) mma16816(scl[kk & 1], A, bql[kk][0], bql[kk][1]);
         }
     } else {
-        uint32_t w0[3], w1[3], c0[4], c1[4];
-        lds_words<3>(r0 + 12 * tig, kmis, w0);
-        lds_words<3>(r1 + 12 * tig, kmis, w1);
-        nibbles3(w0, c0);
-        nibbles3(w1, c1);
+        // one 32-code group (3-bit: 12 bytes, 4-bit: 16 bytes) of each row per
+        // thread, as four nibble words of 8 codes (k-step kk uses 4 of them)
+        uint32_t c0[4], c1[4];
+        if constexpr (KMODE == 3) {
+            uint32_t w0[3], w1[3];
+            lds_words<3>(r0 + 12 * tig, kmis, w0);
+            lds_words<3>(r1 + 12 * tig, kmis, w1);
+            nibbles3(w0, c0);
+            nibbles3(w1, c1);
+        } else {
+            lds_words<4>(r0 + 16 * tig, kmis, c0);
+            lds_words<4>(r1 + 16 * tig, kmis, c1);
+        }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t s0 = c0[kk >> 1] >> (16 * (kk & 1));
             const uint32_t s1 = c1[kk >> 1] >> (16 * (kk & 1));
             uint32_t Ahi[4], Alo[4];
-            {
+            if constexpr (KMODE == 4) {
+                lut16(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
+                lut16(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
+            } else {
+                // 3-bit keys: one lookup per byte plane, then interleave the
+                // low and high bytes into half2 registers
                 const uint32_t p0 = prmt(T[0][0], T[0][1], s0), p1 = prmt(T[1][0], T[1][1], s0);
                 const uint32_t q0 = prmt(T[0][0], T[0][1], s1), q1 = prmt(T[1][0], T[1][1], s1);
                 Ahi[0] = prmt(p0, p1, 0x5140u);
                 Ahi[2] = prmt(p0, p1, 0x7362u);
                 Ahi[1] = prmt(q0, q1, 0x5140u);
                 Ahi[3] = prmt(q0, q1, 0x7362u);
-            }
-            {
-                const uint32_t p0 = prmt(T[2][0], T[2][1], s0), p1 = prmt(T[3][0], T[3][1], s0);
-                const uint32_t q0 = prmt(T[2][0], T[2][1], s1), q1 = prmt(T[3][0], T[3][1], s1);
-                Alo[0] = prmt(p0, p1, 0x5140u);
-                Alo[2] = prmt(p0, p1, 0x7362u);
-                Alo[1] = prmt(q0, q1, 0x5140u);
-                Alo[3] = prmt(q0, q1, 0x7362u);
+                const uint32_t u0 = prmt(T[2][0], T[2][1], s0), u1 = prmt(T[3][0], T[3][1], s0);
+                const uint32_t v0 = prmt(T[2][0], T[2][1], s1), v1 = prmt(T[3][0], T[3][1], s1);
+                Alo[0] = prmt(u0, u1, 0x5140u);
+                Alo[2] = prmt(u0, u1, 0x7362u);
+                Alo[1] = prmt(v0, v1, 0x5140u);
+                Alo[3] = prmt(v0, v1, 0x7362u);
             }
             if constexpr (G == 4) {
                 mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
@@ -352,7 +385,7 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
     }
 }
 
-// KMODE: 8 = FP8 E4M3 keys, 3 = 3-bit Lloyd-Max keys.  VBITS: 3 or 4.
+// KMODE: 8 = FP8 E4M3 keys, 3 / 4 = 3- / 4-bit Lloyd-Max keys.  VBITS: 3 or 4.
 // G: 4 (columns = 4 heads x {hi, lo}) or 8 (columns = 8 heads).
 // One CTA = (split, sequence); warp w = kv head w; each iteration consumes a
 // 32-token tile (two 16-row MMA tiles) with one softmax update.
@@ -500,22 +533,27 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     if (warp == 0)
         for (int i = s_q; i < NST; ++i) issue(i, i);
 
-    // ---------------- centroid byte planes for the PRMT lookup (3-bit keys):
+    // ---------------- centroid byte planes for the PRMT lookup (MSE keys):
     // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
-    // fp16 residual c - fp16(c); [k >> 2] holds entries 4(k>>2) .. 4(k>>2)+3.
-    uint32_t T[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
-    if constexpr (KMODE == 3) {
+    // fp16 residual c - fp16(c).  3-bit keys: T[p][k >> 2] holds entries
+    // 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
+    // plane p of codes 8(k>>3) .. 8(k>>3)+7 in the same way.
+    uint32_t T[KMODE == 4 ? 8 : 4][2] = {};
+    if constexpr (KMODE == 3 || KMODE == 4) {
+        constexpr int NC = KMODE == 3 ? 8 : 16;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < NC; ++k) {
             const float c = a.centroids[k];
             const __half chi = __float2half_rn(c);
             const __half clo = __float2half_rn(c - __half2float(chi));
             const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
-            const int sh = 8 * (k & 3);
-            T[0][k >> 2] |= (hb & 0xFFu) << sh;
-            T[1][k >> 2] |= (hb >> 8) << sh;
-            T[2][k >> 2] |= (lb & 0xFFu) << sh;
-            T[3][k >> 2] |= (lb >> 8) << sh;
+            const int sh = 8 * (k & 3), w = (k >> 2) & 1;
+            const int t = KMODE == 3 ? 0 : (k >> 3);     // table of the plane
+            const int st = KMODE == 3 ? 1 : 2;           // tables per plane
+            T[0 * st + t][w] |= (hb & 0xFFu) << sh;
+            T[1 * st + t][w] |= (hb >> 8) << sh;
+            T[2 * st + t][w] |= (lb & 0xFFu) << sh;
+            T[3 * st + t][w] |= (lb >> 8) << sh;
         }
     }
 
@@ -546,7 +584,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             float sc[4], scl[4];
             qk_tile<KMODE, G>(r0, r1, tig, kmis, bq, bql, T, sc, scl);
             float n0 = 1.f, n1 = 1.f;
-            if constexpr (KMODE == 3) { n0 = lds_f16(r0 + a.g.off_k_norm); n1 = lds_f16(r1 + a.g.off_k_norm); }
+            if constexpr (KMODE != 8) { n0 = lds_f16(r0 + a.g.off_k_norm); n1 = lds_f16(r1 + a.g.off_k_norm); }
             vs[rt][0] = lds_f16(r0 + a.g.off_v_scale);
             vz[rt][0] = lds_f16(r0 + a.g.off_v_zero);
             vs[rt][1] = lds_f16(r1 + a.g.off_v_scale);
@@ -726,6 +764,7 @@ template <typename TQ>
 cudaError_t launch_q(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
 {
     if (a.g.key_fp8) return launch_g<TQ, 8, 4>(a, B, smem, st);
+    if (a.g.key_bits == 4) return launch_g<TQ, 4, 4>(a, B, smem, st);
     if (a.g.value_bits == 4) return launch_g<TQ, 3, 4>(a, B, smem, st);
     return launch_g<TQ, 3, 3>(a, B, smem, st);
 }
@@ -774,7 +813,8 @@ int slots_t(const MmaGeom& m, int num_sms)
 
 bool mma_stage1_supported(const tq_layout& L, int num_kv_heads, int group)
 {
-    const bool keys_ok = (L.key_fp8 && L.value_bits == 4) || (!L.key_fp8 && L.key_bits == 3);
+    const bool keys_ok = (L.key_fp8 && L.value_bits == 4) ||
+                         (!L.key_fp8 && (L.key_bits == 3 || (L.key_bits == 4 && L.value_bits == 4)));
     const bool vals_ok = L.value_bits == 3 || L.value_bits == 4;
     if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > 8) return false;
     const MmaGeom m = mma_geom(L, num_kv_heads, group);
@@ -790,6 +830,7 @@ void mma_stage1_shape(const tq_layout& L, int num_kv_heads, int group, int num_s
     int n = 0;
     if (num_sms > 0) {
         if (L.key_fp8) n = group <= 4 ? slots_t<8, 4, 4>(m, num_sms) : slots_t<8, 4, 8>(m, num_sms);
+        else if (L.key_bits == 4) n = group <= 4 ? slots_t<4, 4, 4>(m, num_sms) : slots_t<4, 4, 8>(m, num_sms);
         else if (L.value_bits == 4) n = group <= 4 ? slots_t<3, 4, 4>(m, num_sms) : slots_t<3, 4, 8>(m, num_sms);
         else n = group <= 4 ? slots_t<3, 3, 4>(m, num_sms) : slots_t<3, 3, 8>(m, num_sms);
     }

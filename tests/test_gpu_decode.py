@@ -52,14 +52,14 @@ CASES = [  # (G, Hk, bs, seq_lens, splits): CUDA-core and tensor-core stage 1 sh
 
 
 def _expected_kind(preset, G, Hk):
-    """Tensor-core stage 1 serves FP8 / 3-bit keys and G <= 8.  A CTA takes
-    the token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above 4) or of
-    all Hk <= 16 heads; that part of a row must be whole 16-byte units and a
+    """Tensor-core stage 1 serves every preset with G <= 8.  A CTA takes the
+    token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above 4) or of all
+    Hk <= 16 heads; that part of a row must be whole 16-byte units and a
     two-stage ring of 32 such rows must fit in ~110 KB of shared memory."""
     slot = [196, 134, 118, 102][preset]
     hpc = 4 if (preset == 0 and Hk % 4 == 0 and Hk > 4) else Hk
     row = hpc * slot
-    return int(preset != 1 and G <= 8 and hpc <= 16 and row % 16 == 0
+    return int(G <= 8 and hpc <= 16 and row % 16 == 0
                and 2 * 32 * (row + 16) <= 110 * 1024)
 
 
