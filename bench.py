@@ -328,6 +328,35 @@ def time_store_mixed(dev):
     return res
 
 
+def time_dequant(p: "Problem", peak_gbs: float, calls: int = 20):
+    """Dequantisation side run: every cached token of the workload back to
+    fp16 K and V (tq_dequant over the whole slot list).  Bytes = slots read +
+    slot mapping + K and V written; outputs and cache together exceed L2."""
+    import torch
+    w = p.w
+    sm = torch.from_numpy(np.concatenate([w.slot_mapping(b, np.arange(int(w.seq_lens[b])))
+                                          for b in range(w.B)])).to(p.dev)
+    N = sm.numel()
+    ko = torch.empty((N, w.Hk, w.D), dtype=torch.float16, device=p.dev)
+    vo = torch.empty_like(ko)
+    for _ in range(3):
+        p.c.dequant(sm, ko, vo)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(calls):
+        p.c.dequant(sm, ko, vo)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / calls
+    nbytes = N * w.Hk * SLOT[w.preset] + 8 * N + 2 * N * w.Hk * w.D * 2
+    del ko, vo
+    torch.cuda.empty_cache()
+    return {"tokens": N, "kv_heads": w.Hk, "out_dtype": "f16", "ms": round(ms, 5),
+            "bytes": nbytes, "gbs": round(nbytes / ms / 1e6, 1),
+            "frac_of_measured_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
+
+
 def time_long_context(dev, peak_gbs: float, ctxs=(32768, 131072), calls: int = 100):
     """Decode-only side run at long contexts: the Llama-3-8B shape (k8v4,
     bs 16) at each context with batch 2^20 / ctx, the library's split count;
@@ -507,6 +536,7 @@ def main():
     if not args.no_extra and rank == 0:
         line["store_mixed"] = time_store_mixed(dev)
         line["store_mtok_s"] = line["store_mixed"]["turboquant_4bit_nc"]["mtok_s"]
+        line["dequant"] = time_dequant(p, peak)
         if args.workload == "llama3_8b" and args.ctx is None and args.batch is None:
             line["long_context"] = time_long_context(dev, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

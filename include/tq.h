@@ -1,9 +1,10 @@
 /*
  * tq.h -- C ABI of the TurboQuant KV-cache hot path on GB300 (sm_103a).
  *
- * Two device operations and the host set-up they need:
+ * The device operations and the host set-up they need:
  *   tq_store            fused quantising store of new K/V tokens into a paged cache
  *   tq_decode_attention split-K decode attention read straight from that cache
+ *   tq_dequant          cached slots back to K/V in the original space
  *   tq_build_codebook, tq_make_signs, tq_get_layout   host set-up
  *
  * Cache layout (one combined K+V slot per (block, token, kv head), no leading
@@ -132,6 +133,31 @@ int tq_store(int preset, int head_dim, int num_tokens, int num_kv_heads, int blo
              const int64_t* slot_mapping, uint8_t* kv_cache, long long num_blocks,
              const int8_t* signs, const float* centroids, const float* midpoints,
              void* stream);
+
+/* Dequantisation of cached slots back to K and V in the original space, the
+ * inverse of tq_store for the slots slot_mapping names ("vllm.v1.attention.
+ * backends.turboquant_attn" API page, "_continuation_prefill": the cached
+ * prefix is dequantised in full and its MSE keys rotated back).  For every
+ * token n < num_tokens and kv head h, from the slot at block
+ * slot_mapping[n] / block_size, offset slot_mapping[n] % block_size:
+ *   MSE keys: k = k_norm * (s . (H c[idx])) with H the orthonormal Sylvester
+ *     Hadamard matrix (the store's rotation undone); FP8 keys: E4M3 decoded.
+ *   Values: v = code * v_scale + v_zero.
+ * Computed in fp32 (fast transform for H) and rounded once to out_dtype.
+ * key_out, value_out: device, element type out_dtype (F16/BF16/F32), element
+ *   (n, h, d) at [n*stride_tok + h*head_dim + d]; both 16-byte aligned, strides
+ *   >= num_kv_heads*head_dim and multiples of 8 elements.
+ * slot_mapping: device int64[num_tokens]; a negative slot or one at or beyond
+ *   num_blocks*block_size gives zero rows and reads nothing.
+ * kv_cache: device, 16-byte aligned, layout as for tq_store.  signs and
+ *   centroids: as for tq_store (ignored, may be NULL, for k8v4).
+ * Supported: head_dim 128, block_size 16/32/64/128.  num_tokens == 0 is a
+ * no-op.  Returns TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED or
+ * TQ_ERR_CUDA. */
+int tq_dequant(int preset, int head_dim, int num_tokens, int num_kv_heads, int block_size,
+               const uint8_t* kv_cache, long long num_blocks, const int64_t* slot_mapping,
+               const int8_t* signs, const float* centroids, void* key_out, void* value_out,
+               int out_dtype, long long key_stride_tok, long long value_stride_tok, void* stream);
 
 /* Split count the library uses when tq_decode_attention gets num_splits = 0,
  * from host-known sizes (no device memory is read; the current device's SM

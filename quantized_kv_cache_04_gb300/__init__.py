@@ -8,13 +8,13 @@ from __future__ import annotations
 
 from . import _lib
 from ._lib import (PRESETS, TQ_3BIT_NC, TQ_4BIT_NC, TQ_BF16, TQ_F16, TQ_F32, TQ_K3V4_NC,
-                   TQ_K8V4, TQError, decode_attention, load, store, tq_build_codebook,
+                   TQ_K8V4, TQError, decode_attention, dequant, load, store, tq_build_codebook,
                    tq_decode_attention, tq_decode_kernel_kind, tq_decode_pick_splits, tq_decode_workspace_bytes,
-                   tq_get_layout, tq_make_signs, tq_status_string, tq_store, tq_version)
+                   tq_dequant, tq_get_layout, tq_make_signs, tq_status_string, tq_store, tq_version)
 
 __all__ = ["PRESETS", "TQ_K8V4", "TQ_4BIT_NC", "TQ_K3V4_NC", "TQ_3BIT_NC", "TQ_F16", "TQ_BF16",
-           "TQ_F32", "TQError", "TQCache", "load", "store", "decode_attention", "tq_store",
-           "tq_decode_attention", "tq_decode_kernel_kind", "tq_get_layout", "tq_build_codebook", "tq_make_signs",
+           "TQ_F32", "TQError", "TQCache", "load", "store", "decode_attention", "dequant", "tq_store",
+           "tq_decode_attention", "tq_dequant", "tq_decode_kernel_kind", "tq_get_layout", "tq_build_codebook", "tq_make_signs",
            "tq_decode_workspace_bytes", "tq_decode_pick_splits", "tq_status_string", "tq_version"]
 
 SIGN_SEED = 42          # per-layer seed = 42 + 1337 * layer
@@ -55,6 +55,11 @@ class TQCache:
         import torch
         nbytes = tq_decode_workspace_bytes(batch, num_q_heads, num_splits, self.head_dim)
         return torch.empty(max(16, nbytes), dtype=torch.uint8, device=self.device)
+
+    def dequant(self, slot_mapping, key_out, value_out, stream=None):
+        """K and V of the slots slot_mapping names, in the original space."""
+        dequant(self.preset, slot_mapping, self.cache, self.num_kv_heads, self.block_size,
+                self.signs, self.centroids, key_out, value_out, stream)
 
     def decode(self, query, block_table, seq_lens, max_seq_len, out, lse, workspace,
                num_splits=0, softmax_scale=None, stream=None):

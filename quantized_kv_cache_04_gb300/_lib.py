@@ -71,6 +71,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                       _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_sz,
                                                       _c_vp])
     L.tq_decode_kernel_kind.argtypes = [_c_int] * 4
+    L.tq_dequant.argtypes = ([_c_int] * 5 + [_c_vp, _c_ll, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int,
+                                             _c_ll, _c_ll, _c_vp])
     L.tq_status_string.argtypes = [_c_int]
     L.tq_status_string.restype = ctypes.c_char_p
     L.tq_version.restype = _c_int
@@ -145,6 +147,11 @@ def tq_decode_attention(*args) -> int:
     return load().tq_decode_attention(*args)
 
 
+def tq_dequant(*args) -> int:
+    """Raw C call; arguments exactly as in include/tq.h.  Returns the status."""
+    return load().tq_dequant(*args)
+
+
 # ------------------------------------------------------------------ torch helpers
 def _dtype_code(t) -> int:
     import torch
@@ -173,6 +180,20 @@ def store(preset: int, key, value, slot_mapping, kv_cache, block_size: int, sign
                   _stream_ptr(stream))
     if rc:
         raise TQError("tq_store", rc)
+
+
+def dequant(preset: int, slot_mapping, kv_cache, num_kv_heads: int, block_size: int, signs,
+            centroids, key_out, value_out, stream=None) -> None:
+    """tq_dequant on torch tensors: key_out/value_out (N, Hk, D) with unit inner strides."""
+    N, Hk, D = key_out.shape
+    assert key_out.stride(2) == 1 and key_out.stride(1) == D
+    assert value_out.stride(2) == 1 and value_out.stride(1) == D and value_out.dtype == key_out.dtype
+    rc = tq_dequant(int(preset), D, N, int(num_kv_heads), int(block_size), _ptr(kv_cache),
+                    kv_cache.shape[0], _ptr(slot_mapping), _ptr(signs), _ptr(centroids),
+                    _ptr(key_out), _ptr(value_out), _dtype_code(key_out), key_out.stride(0),
+                    value_out.stride(0), _stream_ptr(stream))
+    if rc:
+        raise TQError("tq_dequant", rc)
 
 
 def decode_attention(preset: int, query, kv_cache, block_table, seq_lens, max_seq_len: int,

@@ -119,3 +119,29 @@ def test_device_calls_rejected_on_host():
     # decode: empty batch is a no-op
     assert tq.tq_decode_attention(1, 128, 0, 8, 2, 16, 0, z, z, 0, z, 0, z, 0, 0.1, 0, z, z, z,
                                   2, z, z, 0, None) == 0
+
+
+def test_dequant_rejected_on_host():
+    """tq_dequant validates its arguments before any launch."""
+    z, a = 0, 1 << 20                       # a: a 16-byte aligned fake address
+    args = dict(preset=1, hd=128, n=10, hk=8, bs=16, cache=a, nb=4, sm=a, sg=a, c=a, k=a, v=a,
+                dt=0, ks=1024, vs=1024)
+
+    def call(**kw):
+        x = dict(args, **kw)
+        return tq.tq_dequant(x["preset"], x["hd"], x["n"], x["hk"], x["bs"], x["cache"], x["nb"],
+                             x["sm"], x["sg"], x["c"], x["k"], x["v"], x["dt"], x["ks"], x["vs"], None)
+
+    assert call(hd=64) == _lib.TQ_ERR_UNSUPPORTED          # head_dim
+    assert call(bs=8) == _lib.TQ_ERR_UNSUPPORTED           # block size
+    assert call(dt=5) == _lib.TQ_ERR_UNSUPPORTED           # output dtype
+    assert call(preset=9) == _lib.TQ_ERR_UNSUPPORTED       # preset
+    assert call(n=0, cache=z, sm=z, k=z, v=z) == 0         # no tokens: no-op
+    assert call(n=-1) == _lib.TQ_ERR_INVALID_ARG
+    assert call(hk=0) == _lib.TQ_ERR_INVALID_ARG
+    assert call(sm=z) == _lib.TQ_ERR_INVALID_ARG            # null slot mapping
+    assert call(c=z) == _lib.TQ_ERR_INVALID_ARG             # MSE keys need centroids
+    assert call(ks=1000) == _lib.TQ_ERR_INVALID_ARG         # stride below a token row
+    assert call(vs=1028) == _lib.TQ_ERR_INVALID_ARG         # stride not a multiple of 8
+    assert call(k=a + 8) == _lib.TQ_ERR_INVALID_ARG         # output not 16-byte aligned
+    assert call(cache=a + 2) == _lib.TQ_ERR_INVALID_ARG     # cache not 16-byte aligned
