@@ -30,35 +30,51 @@ struct DqArgs {
     SlotGeom g;
 };
 
-constexpr int kDqWarps = 8;           // (token, kv head) pairs per CTA
+constexpr int kDqWarps = 8;           // warps per CTA, one token at a time each
 
-// Codes of dims 4 lane .. 4 lane + 3 from packed data p (2-byte aligned).
-// 4-bit: low nibble first.  3-bit: groups of 32 codes in 12 bytes read as
-// words W0..W2; code 8w + i sits in bits 4i..4i+2 of Ww, and bit w of code
-// 24 + i in bit 4i + 3 of Ww.
+// Raw packed codes of the lane's 4 dims: 4-bit: one 16-bit word; 3-bit: the
+// lane's 32-code group as three 32-bit words.  Loaded in a first phase so
+// that the loads of several pairs are in flight together.
 template <int BITS>
-__device__ __forceinline__ void lane_codes(const uint8_t* p, int lane, int (&c)[4])
+struct RawCodes {
+    uint32_t w[BITS == 4 ? 1 : 3];
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_codes(const uint8_t* p, int lane, RawCodes<BITS>& r)
 {
     if constexpr (BITS == 4) {
-        const uint32_t x = ld_u16(p + 2 * lane);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[i] = (x >> (4 * i)) & 15;
+        r.w[0] = ld_u16(p + 2 * lane);
     } else {
         const uint8_t* grp = p + 12 * (lane >> 3);
-        uint32_t W[3];
 #pragma unroll
-        for (int w = 0; w < 3; ++w) W[w] = uint32_t(ld_u16(grp + 4 * w)) | (uint32_t(ld_u16(grp + 4 * w + 2)) << 16);
+        for (int w = 0; w < 3; ++w)
+            r.w[w] = uint32_t(ld_u16(grp + 4 * w)) | (uint32_t(ld_u16(grp + 4 * w + 2)) << 16);
+    }
+}
+
+// Codes of dims 4 lane .. 4 lane + 3.  4-bit: low nibble first.  3-bit:
+// groups of 32 codes in 12 bytes read as words W0..W2; code 8w + i sits in
+// bits 4i..4i+2 of Ww, and bit w of code 24 + i in bit 4i + 3 of Ww.
+template <int BITS>
+__device__ __forceinline__ void lane_codes(const RawCodes<BITS>& r, int lane, int (&c)[4])
+{
+    if constexpr (BITS == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = (r.w[0] >> (4 * i)) & 15;
+    } else {
         const int j0 = 4 * (lane & 7);          // first code of the lane within its group
         if (j0 < 24) {
-            const uint32_t x = W[j0 >> 3] >> (4 * (j0 & 7));
+            const uint32_t wj = j0 < 8 ? r.w[0] : (j0 < 16 ? r.w[1] : r.w[2]);
+            const uint32_t x = wj >> (4 * (j0 & 7));
 #pragma unroll
             for (int i = 0; i < 4; ++i) c[i] = (x >> (4 * i)) & 7;
         } else {
             const int sh = 4 * (j0 - 24) + 3;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                c[i] = int(((W[0] >> (sh + 4 * i)) & 1) | (((W[1] >> (sh + 4 * i)) & 1) << 1) |
-                           (((W[2] >> (sh + 4 * i)) & 1) << 2));
+                c[i] = int(((r.w[0] >> (sh + 4 * i)) & 1) | (((r.w[1] >> (sh + 4 * i)) & 1) << 1) |
+                           (((r.w[2] >> (sh + 4 * i)) & 1) << 2));
         }
     }
 }
@@ -76,69 +92,143 @@ __device__ __forceinline__ void store4(TO* p, const float (&x)[4])
     }
 }
 
-// One warp per (token, kv head); lane l holds dims 4l .. 4l+3.
+// The slot bytes one lane needs for its 4 dims of one (token, kv head).
 // KBITS: 0 = FP8 keys, 3 or 4 = Lloyd-Max keys.  VBITS: 3 or 4.
+template <int KBITS, int VBITS>
+struct PairRaw {
+    uint32_t kw;                  // FP8 keys: the lane's 4 key bytes
+    RawCodes<KBITS == 0 ? 4 : KBITS> kc;
+    RawCodes<VBITS> vc;
+    uint16_t norm, scale, zero;
+};
+
+template <int KBITS, int VBITS>
+__device__ __forceinline__ void load_pair(const DqArgs& a, const uint8_t* s, int lane, PairRaw<KBITS, VBITS>& r)
+{
+    if constexpr (KBITS == 0) {
+        r.kw = *reinterpret_cast<const uint32_t*>(s + 4 * lane);   // slot 196: 4-byte aligned
+    } else {
+        load_codes<KBITS>(s, lane, r.kc);
+        r.norm = ld_u16(s + a.g.off_k_norm);
+    }
+    load_codes<VBITS>(s + a.g.off_v_data, lane, r.vc);
+    r.scale = ld_u16(s + a.g.off_v_scale);
+    r.zero = ld_u16(s + a.g.off_v_zero);
+}
+
+// Lane l of the warp writes dims 4l .. 4l+3 of one kv head's K and V rows.
+template <typename TO, int KBITS, int VBITS>
+__device__ __forceinline__ void finish_pair(const DqArgs& a, TO* ko, TO* vo, int lane, float cl,
+                                            const float (&sg4)[4], const PairRaw<KBITS, VBITS>& r)
+{
+    float k[4], v[4];
+    if constexpr (KBITS == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half_raw hr = __nv_cvt_fp8_to_halfraw(
+                static_cast<__nv_fp8_storage_t>((r.kw >> (8 * i)) & 0xFF), __NV_E4M3);
+            k[i] = __half2float(__half(hr));
+        }
+    } else {
+        int c[4];
+        lane_codes<KBITS>(r.kc, lane, c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) k[i] = __shfl_sync(0xffffffffu, cl, c[i]);
+        fwht128_warp(k, lane);                   // H c up to the 1/sqrt(D) factor
+        const float f = __half2float(__ushort_as_half(r.norm)) * 0.08838834764831845f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) k[i] = k[i] * f * sg4[i];
+    }
+    {
+        const float sc = __half2float(__ushort_as_half(r.scale));
+        const float z = __half2float(__ushort_as_half(r.zero));
+        int c[4];
+        lane_codes<VBITS>(r.vc, lane, c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = fmaf(float(c[i]), sc, z);   // code * scale is exact in fp32
+    }
+    store4(ko + 4 * lane, k);
+    store4(vo + 4 * lane, v);
+}
+
+// Warps stride over tokens; a warp does every kv head of its token, two
+// heads per step with the slot loads of both issued before either is decoded.
 template <typename TO, int KBITS, int VBITS>
 __global__ void __launch_bounds__(32 * kDqWarps) dequant_kernel(DqArgs a)
 {
     const int lane = threadIdx.x & 31;
-    const long long pair = (long long)blockIdx.x * kDqWarps + (threadIdx.x >> 5);
-    if (pair >= (long long)a.num_tokens * a.Hk) return;
-    const long long n = pair / a.Hk;
-    const int h = int(pair - n * a.Hk);
-    TO* ko = static_cast<TO*>(a.kout) + n * a.k_stride + h * kHeadDim + 4 * lane;
-    TO* vo = static_cast<TO*>(a.vout) + n * a.v_stride + h * kHeadDim + 4 * lane;
-    const long long slot = a.slot_mapping[n];
-    float k[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (slot < 0 || slot >= a.nslots) {        // padding: zero rows, nothing read
-        store4(ko, k);
-        store4(vo, v);
-        return;
-    }
-    const uint8_t* s = a.cache + (slot * a.Hk + h) * a.g.slot;
-
-    if constexpr (KBITS == 0) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(s + 4 * lane);   // slot 196: 4-byte aligned
+    const long long nw = (long long)gridDim.x * kDqWarps;
+    // centroid table in registers: lane j < 2^KBITS holds c[j]; the lane's signs
+    const float cl = (KBITS > 0 && lane < (1 << KBITS)) ? a.centroids[lane] : 0.f;
+    float sg4[4] = {1.f, 1.f, 1.f, 1.f};
+    if constexpr (KBITS > 0) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>((w >> (8 * i)) & 0xFF),
-                                                          __NV_E4M3);
-            k[i] = __half2float(__half(hr));
+        for (int i = 0; i < 4; ++i) sg4[i] = float(a.signs[4 * lane + i]);
+    }
+    const int Hk = a.Hk, S = a.g.slot;
+    for (long long n = (long long)blockIdx.x * kDqWarps + (threadIdx.x >> 5); n < a.num_tokens; n += nw) {
+        const long long slot = a.slot_mapping[n];
+        TO* kr = static_cast<TO*>(a.kout) + n * a.k_stride;
+        TO* vr = static_cast<TO*>(a.vout) + n * a.v_stride;
+        if (slot < 0 || slot >= a.nslots) {     // padding: zero rows, nothing read
+            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int h = 0; h < Hk; ++h) {
+                store4(kr + h * kHeadDim + 4 * lane, z);
+                store4(vr + h * kHeadDim + 4 * lane, z);
+            }
+            continue;
         }
-    } else {
-        // centroid table in registers: lane j < 2^KBITS holds c[j]
-        const float cl = lane < (1 << KBITS) ? a.centroids[lane] : 0.f;
-        int c[4];
-        lane_codes<KBITS>(s, lane, c);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) k[i] = __shfl_sync(0xffffffffu, cl, c[i]);
-        fwht128_warp(k, lane);                   // H c up to the 1/sqrt(D) factor
-        const float norm = __half2float(__ushort_as_half(ld_u16(s + a.g.off_k_norm)));
-        const float f = norm * 0.08838834764831845f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) k[i] = k[i] * f * float(a.signs[4 * lane + i]);
+        const uint8_t* row = a.cache + slot * Hk * S;
+        int h = 0;
+        for (; h + 1 < Hk; h += 2) {
+            PairRaw<KBITS, VBITS> r0, r1;
+            load_pair(a, row + h * S, lane, r0);
+            load_pair(a, row + (h + 1) * S, lane, r1);
+            finish_pair<TO>(a, kr + h * kHeadDim, vr + h * kHeadDim, lane, cl, sg4, r0);
+            finish_pair<TO>(a, kr + (h + 1) * kHeadDim, vr + (h + 1) * kHeadDim, lane, cl, sg4, r1);
+        }
+        if (h < Hk) {
+            PairRaw<KBITS, VBITS> r0;
+            load_pair(a, row + h * S, lane, r0);
+            finish_pair<TO>(a, kr + h * kHeadDim, vr + h * kHeadDim, lane, cl, sg4, r0);
+        }
     }
+}
 
-    {
-        const float sc = __half2float(__ushort_as_half(ld_u16(s + a.g.off_v_scale)));
-        const float z = __half2float(__ushort_as_half(ld_u16(s + a.g.off_v_zero)));
-        int c[4];
-        lane_codes<VBITS>(s + a.g.off_v_data, lane, c);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = fmaf(float(c[i]), sc, z);   // code * scale is exact in fp32
+// One wave of resident CTAs (occupancy of this instantiation on the current
+// device, asked once), or fewer when there are fewer tokens.
+template <typename TO, int KBITS, int VBITS>
+cudaError_t launch_one(const DqArgs& a, long long tokens, cudaStream_t st)
+{
+    static int resident[64];                 // per device: CTAs per SM x SMs, 0 until asked
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int* res = dev >= 0 && dev < 64 ? &resident[dev] : nullptr;
+    int n = res ? *res : 0;
+    if (n <= 0) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dequant_kernel<TO, KBITS, VBITS>,
+                                                              32 * kDqWarps, 0);
+        if (e != cudaSuccess) return e;
+        n = per_sm > 0 && sms > 0 ? per_sm * sms : 1;
+        if (res) *res = n;                   // the same value from any thread
     }
-    store4(ko, k);
-    store4(vo, v);
+    long long grid = (tokens + kDqWarps - 1) / kDqWarps;
+    if (grid > n) grid = n;
+    dequant_kernel<TO, KBITS, VBITS><<<unsigned(grid), 32 * kDqWarps, 0, st>>>(a);
+    return cudaGetLastError();
 }
 
 template <typename TO>
-cudaError_t launch_dq(const DqArgs& a, unsigned grid, cudaStream_t st)
+cudaError_t launch_dq(const DqArgs& a, long long tokens, cudaStream_t st)
 {
-    if (a.g.key_fp8) dequant_kernel<TO, 0, 4><<<grid, 32 * kDqWarps, 0, st>>>(a);
-    else if (a.g.key_bits == 4) dequant_kernel<TO, 4, 4><<<grid, 32 * kDqWarps, 0, st>>>(a);
-    else if (a.g.value_bits == 4) dequant_kernel<TO, 3, 4><<<grid, 32 * kDqWarps, 0, st>>>(a);
-    else dequant_kernel<TO, 3, 3><<<grid, 32 * kDqWarps, 0, st>>>(a);
-    return cudaGetLastError();
+    if (a.g.key_fp8) return launch_one<TO, 0, 4>(a, tokens, st);
+    if (a.g.key_bits == 4) return launch_one<TO, 4, 4>(a, tokens, st);
+    if (a.g.value_bits == 4) return launch_one<TO, 3, 4>(a, tokens, st);
+    return launch_one<TO, 3, 3>(a, tokens, st);
 }
 
 }  // namespace
@@ -180,12 +270,9 @@ extern "C" int tq_dequant(int preset, int head_dim, int num_tokens, int num_kv_h
     a.k_stride = key_stride_tok;
     a.v_stride = value_stride_tok;
     a.g = geom_of(L);
-    const long long pairs = (long long)num_tokens * num_kv_heads;
-    const long long grid = (pairs + kDqWarps - 1) / kDqWarps;
-    if (grid > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = out_dtype == TQ_F32 ? launch_dq<float>(a, unsigned(grid), st)
-                          : out_dtype == TQ_F16 ? launch_dq<__half>(a, unsigned(grid), st)
-                                                : launch_dq<__nv_bfloat16>(a, unsigned(grid), st);
+    const cudaError_t e = out_dtype == TQ_F32 ? launch_dq<float>(a, num_tokens, st)
+                          : out_dtype == TQ_F16 ? launch_dq<__half>(a, num_tokens, st)
+                                                : launch_dq<__nv_bfloat16>(a, num_tokens, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
