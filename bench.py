@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 from quantized_kv_cache_04_gb300 import workloads as wl  # noqa: E402
 
 SLOT = {"turboquant_k8v4": 196, "turboquant_4bit_nc": 134, "turboquant_k3v4_nc": 118,
-        "turboquant_3bit_nc": 102}
+        "turboquant_3bit_nc": 102, "turboquant_2bit_nc": 70}
 L2_BYTES = 129 * 2**20
 NOMINAL_HBM_GBS = 8000.0
 
@@ -357,14 +357,16 @@ def time_dequant(p: "Problem", peak_gbs: float, calls: int = 20):
             "frac_of_measured_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
 
 
-def time_long_context(dev, peak_gbs: float, ctxs=(32768, 131072), calls: int = 100):
-    """Decode-only side run at long contexts: the Llama-3-8B shape (k8v4,
-    bs 16) at each context with batch 2^20 / ctx, the library's split count;
-    mean decode-call time over `calls` back-to-back calls (inputs > L2)."""
+def time_long_context(dev, peak_gbs: float, ctxs=(32768, 262144), presets=tuple(SLOT),
+                      calls: int = 50):
+    """Decode-only side run at long contexts: the Llama-3-8B shape (bs 16)
+    for every preset at each context with batch 2^20 / ctx, the library's
+    split count; mean decode-call time over `calls` back-to-back calls
+    (inputs > L2)."""
     import torch
     res = []
-    for ctx in ctxs:
-        w = wl.make("sweep", ctx=ctx)
+    for ctx, preset in [(c, pr) for pr in presets for c in ctxs]:
+        w = wl.make("sweep", ctx=ctx, preset=preset)
         p = Problem(w, dev, None)
         for _ in range(5):
             p.decode()

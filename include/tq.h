@@ -47,12 +47,16 @@ extern "C" {
 #endif
 
 /* Cache presets: the four cache dtypes of "vllm-project/vllm pull 38479"
- * digest, section "turboquant_attn.py" (supported_kv_cache_dtypes).
+ * digest, section "turboquant_attn.py" (supported_kv_cache_dtypes), and the
+ * 2-bit Lloyd-Max codebook "Turbo2" of "turboquant-plus.md" (feature table),
+ * here in the same slot form as the _nc presets.
  *   TQ_K8V4     FP8 E4M3 keys, 4-bit uniform values               slot 196 B @ D=128
  *   TQ_4BIT_NC  4-bit Lloyd-Max keys + norm correction, 4-bit V  slot 134 B
  *   TQ_K3V4_NC  3-bit Lloyd-Max keys + norm correction, 4-bit V  slot 118 B
- *   TQ_3BIT_NC  3-bit Lloyd-Max keys + norm correction, 3-bit V  slot 102 B */
-typedef enum { TQ_K8V4 = 0, TQ_4BIT_NC = 1, TQ_K3V4_NC = 2, TQ_3BIT_NC = 3 } tq_preset;
+ *   TQ_3BIT_NC  3-bit Lloyd-Max keys + norm correction, 3-bit V  slot 102 B
+ *   TQ_2BIT_NC  2-bit Lloyd-Max keys + norm correction, 2-bit V  slot  70 B
+ * 2-bit codes: four per byte, LSB first. */
+typedef enum { TQ_K8V4 = 0, TQ_4BIT_NC = 1, TQ_K3V4_NC = 2, TQ_3BIT_NC = 3, TQ_2BIT_NC = 4 } tq_preset;
 
 /* Element types of K/V/Q inputs and of the attention output. */
 typedef enum { TQ_F16 = 0, TQ_BF16 = 1, TQ_F32 = 2 } tq_dtype;

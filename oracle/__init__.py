@@ -24,9 +24,10 @@ _SRC = os.path.join(_HERE, "tq_oracle.c")
 _HDR = os.path.join(_HERE, "tq_oracle.h")
 _OUT = os.path.join(_HERE, "_build", "liboracle.so")
 
-K8V4, TQ4_NC, K3V4_NC, TQ3_NC = 0, 1, 2, 3
+K8V4, TQ4_NC, K3V4_NC, TQ3_NC, TQ2_NC = 0, 1, 2, 3, 4
 PRESETS = {"turboquant_k8v4": K8V4, "turboquant_4bit_nc": TQ4_NC,
-           "turboquant_k3v4_nc": K3V4_NC, "turboquant_3bit_nc": TQ3_NC}
+           "turboquant_k3v4_nc": K3V4_NC, "turboquant_3bit_nc": TQ3_NC,
+           "turboquant_2bit_nc": TQ2_NC}
 
 
 def build(force: bool = False) -> str:

@@ -33,6 +33,7 @@ int orc_get_layout(int preset, int D, orc_layout* L)
     case ORC_4BIT_NC: L->key_fp8 = 0; L->key_bits = 4; L->value_bits = 4; L->norm_correction = 1; break;
     case ORC_K3V4_NC: L->key_fp8 = 0; L->key_bits = 3; L->value_bits = 4; L->norm_correction = 1; break;
     case ORC_3BIT_NC: L->key_fp8 = 0; L->key_bits = 3; L->value_bits = 3; L->norm_correction = 1; break;
+    case ORC_2BIT_NC: L->key_fp8 = 0; L->key_bits = 2; L->value_bits = 2; L->norm_correction = 1; break;
     default: return -1;
     }
     int pos = 0;

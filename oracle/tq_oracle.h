@@ -32,6 +32,7 @@ extern "C" {
 #define ORC_4BIT_NC 1
 #define ORC_K3V4_NC 2
 #define ORC_3BIT_NC 3
+#define ORC_2BIT_NC 4   /* Turbo2: 2-bit Lloyd-Max keys + norm correction, 2-bit values */
 
 /* Slot layout derived from [vLLM-API] "__init__" (mse bytes / value data
  * bytes formulas) and [vLLM-API] "_continuation_prefill" (field order

@@ -13,12 +13,13 @@ import os
 
 from . import build as _build
 
-TQ_K8V4, TQ_4BIT_NC, TQ_K3V4_NC, TQ_3BIT_NC = 0, 1, 2, 3
+TQ_K8V4, TQ_4BIT_NC, TQ_K3V4_NC, TQ_3BIT_NC, TQ_2BIT_NC = 0, 1, 2, 3, 4
 TQ_F16, TQ_BF16, TQ_F32 = 0, 1, 2
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA = 0, -1, -2, -3, -4
 TQ_MAX_SPLITS = 256
 PRESETS = {"turboquant_k8v4": TQ_K8V4, "turboquant_4bit_nc": TQ_4BIT_NC,
-           "turboquant_k3v4_nc": TQ_K3V4_NC, "turboquant_3bit_nc": TQ_3BIT_NC}
+           "turboquant_k3v4_nc": TQ_K3V4_NC, "turboquant_3bit_nc": TQ_3BIT_NC,
+           "turboquant_2bit_nc": TQ_2BIT_NC}
 
 _c_int, _c_ll, _c_sz, _c_vp = ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t, ctypes.c_void_p
 

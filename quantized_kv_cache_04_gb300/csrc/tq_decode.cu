@@ -45,18 +45,22 @@ struct DecodeArgs {
 constexpr int kWarps = 4;
 
 // Codes 4*lane .. 4*lane+3 of a packed code stream starting at p (2-byte
-// aligned).  4 bits: low nibble first.  3 bits: 32-code groups of three
-// 32-bit words W0..W2, code 8w+i in bits [4i, 4i+3) of Ww, bit w of code
-// 24+i in bit 4i+3 of Ww.
+// aligned).  4 bits: low nibble first.  2 bits: four per byte, LSB first.
+// 3 bits: 32-code groups of three 32-bit words W0..W2, code 8w+i in bits
+// [4i, 4i+3) of Ww, bit w of code 24+i in bit 4i+3 of Ww.
 template <int BITS>
 __device__ __forceinline__ void load_codes(const uint8_t* p, int lane, int (&c)[4])
 {
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+        const uint32_t w = p[lane];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = (w >> (2 * i)) & 3u;
+    } else if constexpr (BITS == 4) {
         const uint32_t w = ld_u16(p + 2 * lane);
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[i] = (w >> (4 * i)) & 15u;
     } else {
-        static_assert(BITS == 3, "3 or 4 bits");
+        static_assert(BITS == 3, "2, 3 or 4 bits");
         const int j = lane & 7;
         const uint8_t* g = p + 12 * (lane >> 3);
         if (j < 6) {
@@ -308,6 +312,7 @@ cudaError_t launch_stage1(int preset, const DecodeArgs& a, cudaStream_t st)
     case TQ_4BIT_NC: return launch_stage1_g<TQ, false, 4, 4>(a, st);
     case TQ_K3V4_NC: return launch_stage1_g<TQ, false, 3, 4>(a, st);
     case TQ_3BIT_NC: return launch_stage1_g<TQ, false, 3, 3>(a, st);
+    case TQ_2BIT_NC: return launch_stage1_g<TQ, false, 2, 2>(a, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -355,6 +360,7 @@ void stage1_shape(const tq_layout& L, int Hk, int G, int* cps, int* slots)
     } else if (num_sms > 0) {
         c = Hk;                    // grid (splits, kv heads, batch)
         if (L.key_fp8) n = v1_slots<true, 4, 4>(G, num_sms);
+        else if (L.key_bits == 2) n = v1_slots<false, 2, 2>(G, num_sms);
         else if (L.key_bits == 4) n = v1_slots<false, 4, 4>(G, num_sms);
         else if (L.value_bits == 4) n = v1_slots<false, 3, 4>(G, num_sms);
         else n = v1_slots<false, 3, 3>(G, num_sms);

@@ -252,6 +252,20 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
             lds_words<3>(r1 + 12 * tig, kmis, w1);
             nibbles3(w0, c0);
             nibbles3(w1, c1);
+        } else if constexpr (KMODE == 2) {
+            // 32 two-bit codes = two words; the even codes of a word go to one
+            // nibble word and the odd codes to another (code 2i / 2i + 1 of
+            // the word in nibble i), so k-step kk covers dims with stride 2
+            uint32_t w0[2], w1[2];
+            lds_words<2>(r0 + 8 * tig, kmis, w0);
+            lds_words<2>(r1 + 8 * tig, kmis, w1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                c0[2 * i] = w0[i] & 0x33333333u;
+                c0[2 * i + 1] = (w0[i] >> 2) & 0x33333333u;
+                c1[2 * i] = w1[i] & 0x33333333u;
+                c1[2 * i + 1] = (w1[i] >> 2) & 0x33333333u;
+            }
         } else {
             lds_words<4>(r0 + 16 * tig, kmis, c0);
             lds_words<4>(r1 + 16 * tig, kmis, c1);
@@ -265,8 +279,8 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
                 lut16(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
                 lut16(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
             } else {
-                // 3-bit keys: one lookup per byte plane, then interleave the
-                // low and high bytes into half2 registers
+                // 2- and 3-bit keys: one lookup per byte plane, then interleave
+                // the low and high bytes into half2 registers
                 const uint32_t p0 = prmt(T[0][0], T[0][1], s0), p1 = prmt(T[1][0], T[1][1], s0);
                 const uint32_t q0 = prmt(T[0][0], T[0][1], s1), q1 = prmt(T[1][0], T[1][1], s1);
                 Ahi[0] = prmt(p0, p1, 0x5140u);
@@ -355,6 +369,11 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
         const uint8_t* rv = tile_v + (4 * tig + j) * rs;
         if constexpr (VBITS == 4) {
             lds_words<2, ALIGNED>(rv + 8 * gid, vmis, vw[j]);
+        } else if constexpr (VBITS == 2) {
+            uint32_t w[1];
+            lds_words<1, ALIGNED>(rv + 4 * gid, vmis, w);
+            vw[j][0] = w[0];
+            vw[j][1] = 0u;
         } else {
             uint32_t w[3], n[4];
             lds_words<3, ALIGNED>(rv + 12 * (gid >> 1), vmis, w);
@@ -367,6 +386,31 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
     // ab = [A_i, B_i, A_i+1, B_i+1] with A, B the tokens of k = 2 tig, 2 tig + 1
     // (cd likewise for tokens 4 tig + 2, + 3); its low nibbles give row gid
     // (even dims), its high nibbles row gid + 8 (odd dims).
+    if constexpr (VBITS == 2) {
+        // byte b of a token's word holds dims 16 gid + 4b .. 4b + 3 (two bits
+        // each): ab = [A_b, B_b, A_b+1, B_b+1] feeds MMAs 2b .. 2b + 3
+#pragma unroll
+        for (int i = 0; i < 8; i += 4) {
+            const uint32_t c = uint32_t(i >> 1);
+            const uint32_t sel = c | ((c + 4) << 4) | ((c + 1) << 8) | ((c + 5) << 12);
+            const uint32_t ab = prmt(vw[0][0], vw[1][0], sel);
+            const uint32_t cd = prmt(vw[2][0], vw[3][0], sel);
+            uint32_t A[4][4];            // MMAs i .. i + 3
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // two-bit field q of each byte: dim 2i + q (+4 in the high half)
+                const uint32_t m = 0x03030303u;
+                const int mma = (q >> 1), row = q & 1;
+                cvt_e4m3x4((ab >> (2 * q)) & m, A[mma][row], A[mma + 2][row]);
+                cvt_e4m3x4((cd >> (2 * q)) & m, A[mma][row + 2], A[mma + 2][row + 2]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                mma16816(acc[i + u], A[u], pb[0][0], pb[0][1]);
+                if constexpr (G == 8) mma16816(acc[i + u], A[u], pb[1][0], pb[1][1]);
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
         const uint32_t c = uint32_t(i & 3);
@@ -385,7 +429,8 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
     }
 }
 
-// KMODE: 8 = FP8 E4M3 keys, 3 / 4 = 3- / 4-bit Lloyd-Max keys.  VBITS: 3 or 4.
+// KMODE: 8 = FP8 E4M3 keys, 2 / 3 / 4 = 2- / 3- / 4-bit Lloyd-Max keys.
+// VBITS: 2, 3 or 4.
 // G: 4 (columns = 4 heads x {hi, lo}) or 8 (columns = 8 heads).
 // One CTA = (split, sequence); warp w = kv head w; each iteration consumes a
 // 32-token tile (two 16-row MMA tiles) with one softmax update.
@@ -482,6 +527,9 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     //   FP8 keys:   16 kk + 4 tig + j   one key word per k-step, bank-conflict
     //               free across the warp
     //   3-bit keys: 32 tig + 4 kk + j   one 32-code group (three words) per thread
+    //   4-bit keys: the same, 16 bytes per thread
+    //   2-bit keys: 32 tig + 16 (kk >> 2) + 8 (kk & 1) + ((kk >> 1) & 1) + 2 j
+    //               (8 bytes per thread; see qk_tile)
     uint32_t bq[8][2], bql[8][2];
     {
         float* sq = reinterpret_cast<float*>(smem + q_base) + warp * G * kHeadDim;
@@ -511,7 +559,14 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         const float* qc = sq + col_head * kHeadDim;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const float4 x = reinterpret_cast<const float4*>(qc + (KMODE == 8 ? 16 * kk + 4 * tig : 32 * tig + 4 * kk))[0];
+            float4 x;
+            if constexpr (KMODE == 2) {
+                // dims 32 tig + 16 (kk >> 2) + 8 (kk & 1) + ((kk >> 1) & 1) + 2 j
+                const float* qd = qc + 32 * tig + 16 * (kk >> 2) + 8 * (kk & 1) + ((kk >> 1) & 1);
+                x = make_float4(qd[0], qd[2], qd[4], qd[6]);
+            } else {
+                x = reinterpret_cast<const float4*>(qc + (KMODE == 8 ? 16 * kk + 4 * tig : 32 * tig + 4 * kk))[0];
+            }
             float hi[4], lo[4];
             split_f16(x.x, hi[0], lo[0]);
             split_f16(x.y, hi[1], lo[1]);
@@ -535,12 +590,12 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 
     // ---------------- centroid byte planes for the PRMT lookup (MSE keys):
     // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
-    // fp16 residual c - fp16(c).  3-bit keys: T[p][k >> 2] holds entries
+    // fp16 residual c - fp16(c).  2- and 3-bit keys: T[p][k >> 2] holds entries
     // 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
     // plane p of codes 8(k>>3) .. 8(k>>3)+7 in the same way.
     uint32_t T[KMODE == 4 ? 8 : 4][2] = {};
-    if constexpr (KMODE == 3 || KMODE == 4) {
-        constexpr int NC = KMODE == 3 ? 8 : 16;
+    if constexpr (KMODE != 8) {
+        constexpr int NC = 1 << KMODE;
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
             const float c = a.centroids[k];
@@ -548,8 +603,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const __half clo = __float2half_rn(c - __half2float(chi));
             const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
             const int sh = 8 * (k & 3), w = (k >> 2) & 1;
-            const int t = KMODE == 3 ? 0 : (k >> 3);     // table of the plane
-            const int st = KMODE == 3 ? 1 : 2;           // tables per plane
+            const int t = KMODE == 4 ? (k >> 3) : 0;     // table of the plane
+            const int st = KMODE == 4 ? 2 : 1;           // tables per plane
             T[0 * st + t][w] |= (hb & 0xFFu) << sh;
             T[1 * st + t][w] |= (hb >> 8) << sh;
             T[2 * st + t][w] |= (lb & 0xFFu) << sh;
@@ -765,6 +820,7 @@ cudaError_t launch_q(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
 {
     if (a.g.key_fp8) return launch_g<TQ, 8, 4>(a, B, smem, st);
     if (a.g.key_bits == 4) return launch_g<TQ, 4, 4>(a, B, smem, st);
+    if (a.g.key_bits == 2) return launch_g<TQ, 2, 2>(a, B, smem, st);
     if (a.g.value_bits == 4) return launch_g<TQ, 3, 4>(a, B, smem, st);
     return launch_g<TQ, 3, 3>(a, B, smem, st);
 }
@@ -814,8 +870,9 @@ int slots_t(const MmaGeom& m, int num_sms)
 bool mma_stage1_supported(const tq_layout& L, int num_kv_heads, int group)
 {
     const bool keys_ok = (L.key_fp8 && L.value_bits == 4) ||
-                         (!L.key_fp8 && (L.key_bits == 3 || (L.key_bits == 4 && L.value_bits == 4)));
-    const bool vals_ok = L.value_bits == 3 || L.value_bits == 4;
+                         (!L.key_fp8 && (L.key_bits == 3 || (L.key_bits == 4 && L.value_bits == 4) ||
+                                         (L.key_bits == 2 && L.value_bits == 2)));
+    const bool vals_ok = L.value_bits >= 2 && L.value_bits <= 4;
     if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > 8) return false;
     const MmaGeom m = mma_geom(L, num_kv_heads, group);
     const int row = m.copy_bytes;
@@ -831,6 +888,7 @@ void mma_stage1_shape(const tq_layout& L, int num_kv_heads, int group, int num_s
     if (num_sms > 0) {
         if (L.key_fp8) n = group <= 4 ? slots_t<8, 4, 4>(m, num_sms) : slots_t<8, 4, 8>(m, num_sms);
         else if (L.key_bits == 4) n = group <= 4 ? slots_t<4, 4, 4>(m, num_sms) : slots_t<4, 4, 8>(m, num_sms);
+        else if (L.key_bits == 2) n = group <= 4 ? slots_t<2, 2, 4>(m, num_sms) : slots_t<2, 2, 8>(m, num_sms);
         else if (L.value_bits == 4) n = group <= 4 ? slots_t<3, 4, 4>(m, num_sms) : slots_t<3, 4, 8>(m, num_sms);
         else n = group <= 4 ? slots_t<3, 3, 4>(m, num_sms) : slots_t<3, 3, 8>(m, num_sms);
     }

@@ -37,13 +37,15 @@ constexpr int kDqWarps = 8;           // warps per CTA, one token at a time each
 // that the loads of several pairs are in flight together.
 template <int BITS>
 struct RawCodes {
-    uint32_t w[BITS == 4 ? 1 : 3];
+    uint32_t w[BITS == 3 ? 3 : 1];
 };
 
 template <int BITS>
 __device__ __forceinline__ void load_codes(const uint8_t* p, int lane, RawCodes<BITS>& r)
 {
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+        r.w[0] = p[lane];
+    } else if constexpr (BITS == 4) {
         r.w[0] = ld_u16(p + 2 * lane);
     } else {
         const uint8_t* grp = p + 12 * (lane >> 3);
@@ -53,13 +55,17 @@ __device__ __forceinline__ void load_codes(const uint8_t* p, int lane, RawCodes<
     }
 }
 
-// Codes of dims 4 lane .. 4 lane + 3.  4-bit: low nibble first.  3-bit:
+// Codes of dims 4 lane .. 4 lane + 3.  2-bit: four per byte, LSB first.
+// 4-bit: low nibble first.  3-bit:
 // groups of 32 codes in 12 bytes read as words W0..W2; code 8w + i sits in
 // bits 4i..4i+2 of Ww, and bit w of code 24 + i in bit 4i + 3 of Ww.
 template <int BITS>
 __device__ __forceinline__ void lane_codes(const RawCodes<BITS>& r, int lane, int (&c)[4])
 {
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = (r.w[0] >> (2 * i)) & 3;
+    } else if constexpr (BITS == 4) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[i] = (r.w[0] >> (4 * i)) & 15;
     } else {
@@ -93,7 +99,7 @@ __device__ __forceinline__ void store4(TO* p, const float (&x)[4])
 }
 
 // The slot bytes one lane needs for its 4 dims of one (token, kv head).
-// KBITS: 0 = FP8 keys, 3 or 4 = Lloyd-Max keys.  VBITS: 3 or 4.
+// KBITS: 0 = FP8 keys, 2, 3 or 4 = Lloyd-Max keys.  VBITS: 2, 3 or 4.
 template <int KBITS, int VBITS>
 struct PairRaw {
     uint32_t kw;                  // FP8 keys: the lane's 4 key bytes
@@ -227,6 +233,7 @@ cudaError_t launch_dq(const DqArgs& a, long long tokens, cudaStream_t st)
 {
     if (a.g.key_fp8) return launch_one<TO, 0, 4>(a, tokens, st);
     if (a.g.key_bits == 4) return launch_one<TO, 4, 4>(a, tokens, st);
+    if (a.g.key_bits == 2) return launch_one<TO, 2, 2>(a, tokens, st);
     if (a.g.value_bits == 4) return launch_one<TO, 3, 4>(a, tokens, st);
     return launch_one<TO, 3, 3>(a, tokens, st);
 }

@@ -22,6 +22,7 @@ int fill_layout(int preset, int head_dim, tq_layout* L)
     case TQ_4BIT_NC: L->key_bits = 4; L->value_bits = 4; L->norm_correction = 1; break;
     case TQ_K3V4_NC: L->key_bits = 3; L->value_bits = 4; L->norm_correction = 1; break;
     case TQ_3BIT_NC: L->key_bits = 3; L->value_bits = 3; L->norm_correction = 1; break;
+    case TQ_2BIT_NC: L->key_bits = 2; L->value_bits = 2; L->norm_correction = 1; break;
     default: return TQ_ERR_UNSUPPORTED;
     }
     const int D = head_dim;

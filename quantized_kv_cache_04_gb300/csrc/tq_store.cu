@@ -193,6 +193,7 @@ cudaError_t launch_store_t(int preset, const StoreArgs& a, cudaStream_t st)
     case TQ_4BIT_NC: store_kernel<T, false, 4, 4, true><<<grid, threads, smem, st>>>(a); break;
     case TQ_K3V4_NC: store_kernel<T, false, 3, 4, true><<<grid, threads, smem, st>>>(a); break;
     case TQ_3BIT_NC: store_kernel<T, false, 3, 3, true><<<grid, threads, smem, st>>>(a); break;
+    case TQ_2BIT_NC: store_kernel<T, false, 2, 2, true><<<grid, threads, smem, st>>>(a); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

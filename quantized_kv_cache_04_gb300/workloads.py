@@ -19,7 +19,7 @@ import math
 import numpy as np
 
 PRESET_IDS = {"turboquant_k8v4": 0, "turboquant_4bit_nc": 1,
-              "turboquant_k3v4_nc": 2, "turboquant_3bit_nc": 3}
+              "turboquant_k3v4_nc": 2, "turboquant_3bit_nc": 3, "turboquant_2bit_nc": 4}
 PRESET_NAMES = {v: k for k, v in PRESET_IDS.items()}
 SIGN_SEED = 42
 

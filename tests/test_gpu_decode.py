@@ -9,7 +9,7 @@ import quantized_kv_cache_04_gb300 as tq
 from _helpers import check_decode, codebook, paged_problem, to_f32
 
 pytestmark = pytest.mark.gpu
-PRESETS = [0, 1, 2, 3]
+PRESETS = [0, 1, 2, 3, 4]
 
 
 def _gpu_decode(preset, q, cache_np, bt, seq_lens, Hk, bs, signs, c32, num_splits=0,
@@ -56,7 +56,7 @@ def _expected_kind(preset, G, Hk):
     token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above 4) or of all
     Hk <= 16 heads; that part of a row must be whole 16-byte units and a
     two-stage ring of 32 such rows must fit in ~110 KB of shared memory."""
-    slot = [196, 134, 118, 102][preset]
+    slot = [196, 134, 118, 102, 70][preset]
     hpc = 4 if (preset == 0 and Hk % 4 == 0 and Hk > 4) else Hk
     row = hpc * slot
     return int(G <= 8 and hpc <= 16 and row % 16 == 0

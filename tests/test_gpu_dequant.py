@@ -73,7 +73,7 @@ def _check_rows(orc, preset, cache_np, slots, Hk, bs, signs, c32, k, v, out_dtyp
                 assert np.all(verr <= _ulp(vh, out_dtype)), f"row {n} head {h}: values"
 
 
-@pytest.mark.parametrize("preset", [0, 1, 2, 3])
+@pytest.mark.parametrize("preset", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("Hk,bs", [(1, 16), (8, 64), (3, 32)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
 def test_dequant_on_oracle_cache(orc, preset, Hk, bs, out_dtype):
@@ -92,7 +92,7 @@ def test_dequant_on_oracle_cache(orc, preset, Hk, bs, out_dtype):
     _check_rows(orc, preset, pb["cache"], slots, Hk, bs, pb["signs"], pb["c32"], k, v, out_dtype)
 
 
-@pytest.mark.parametrize("preset", [0, 1, 2, 3])
+@pytest.mark.parametrize("preset", [0, 1, 2, 3, 4])
 def test_dequant_inverts_store_up_to_quantisation(orc, preset):
     """A property that holds at any size: FP8 keys come back within E4M3
     rounding of the stored bf16-exact inputs; MSE keys keep the input norm

@@ -11,7 +11,7 @@ import quantized_kv_cache_04_gb300 as tq
 from _helpers import TIE_FRACTION, codebook, compare_store, to_f32
 
 pytestmark = pytest.mark.gpu
-PRESETS = [0, 1, 2, 3]
+PRESETS = [0, 1, 2, 3, 4]
 SENTINEL = 0x5A
 
 

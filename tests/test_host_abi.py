@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_layout_matches_oracle(orc):
-    for p in range(4):
+    for p in range(5):
         a = tq.tq_get_layout(p, 128)
         b = orc.layout(p, 128)
         for k in ("key_fp8", "key_bits", "value_bits", "norm_correction", "key_data_bytes",
@@ -40,7 +40,7 @@ def test_layout_matches_oracle(orc):
                   "slot_size_aligned"):
             assert a[k] == b[k], (p, k)
         assert a["off_k_norm"] == b["off_k_norm"]
-    assert [tq.tq_get_layout(p)["slot_size_aligned"] for p in range(4)] == [196, 134, 118, 102]
+    assert [tq.tq_get_layout(p)["slot_size_aligned"] for p in range(5)] == [196, 134, 118, 102, 70]
     with pytest.raises(tq.TQError):
         tq.tq_get_layout(7, 128)
     with pytest.raises(tq.TQError):
@@ -64,7 +64,7 @@ def test_signs_match_oracle(orc):
 def test_sizing():
     assert tq.tq_decode_workspace_bytes(32, 32, 16, 128) == 32 * 32 * 16 * 129 * 4
     assert tq.tq_decode_workspace_bytes(0, 32, 16, 128) == 0
-    for preset in range(4):
+    for preset in range(5):
         for B, Hk, L in [(1, 2, 512), (32, 8, 8192), (4, 8, 262144), (64, 8, 32768), (1, 1, 1),
                          (0, 8, 100), (3, 8, 0)]:
             s = tq.tq_decode_pick_splits(preset, 128, B, Hk * 4, Hk, L)

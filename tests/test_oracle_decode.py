@@ -4,7 +4,7 @@ split-K/LUT form against the dense form, and closed-form special cases."""
 import numpy as np
 import pytest
 
-PRESETS = [0, 1, 2, 3]
+PRESETS = [0, 1, 2, 3, 4]
 
 
 def _cache(orc, preset, seq_lens, Hk, bs, rng, scale_k=1.0, kind="normal"):

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
-PRESETS = [0, 1, 2, 3]
+PRESETS = [0, 1, 2, 3, 4]
 
 
 def _page_numbers():
@@ -22,7 +22,7 @@ def _page_numbers():
 
 def test_slot_sizes(orc):
     sizes = [orc.layout(p)["slot_size_aligned"] for p in PRESETS]
-    assert sizes == [196, 134, 118, 102]
+    assert sizes == [196, 134, 118, 102, 70]
     ratio = 2 * 128 * 2 / sizes[0]
     assert round(ratio, 1) == _page_numbers()["k8v4_compression"]
     for p in PRESETS:
