@@ -219,6 +219,29 @@ int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,
                         void* out, int out_dtype, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* tq_decode_attention with the sparse-V row skip ("turboquant-plus.md",
+ * feature table: sparse V dequant, an attention-gated row skip).  Arguments
+ * as tq_decode_attention plus v_threshold in [0, 1).  In stage 1 a token row
+ * whose softmax factor p = exp(logit - m) is at most v_threshold, with m the
+ * split's running reference max when the row is processed (never above the
+ * split's final max), keeps its weight in the softmax denominator but adds
+ * nothing to the value sum; the tensor-core kernel skips the value MMAs of a
+ * 16-row tile that keeps no row, the CUDA-core kernel skips the value codes
+ * of such a row.  v_threshold = 0 is tq_decode_attention exactly.  An
+ * approximation: per output dimension the result moves from the dense one by
+ * at most sum_{t: exp(logit_t - M) <= v_threshold} p_t |v_t| / sum_t p_t
+ * (M the sequence's largest logit); the LSE is unchanged.  Returns as
+ * tq_decode_attention, and TQ_ERR_INVALID_ARG for a threshold outside
+ * [0, 1). */
+int tq_decode_attention_sparse_v(int preset, int head_dim, int batch, int num_q_heads,
+                                 int num_kv_heads, int block_size, int q_dtype, const void* query,
+                                 const uint8_t* kv_cache, long long num_blocks,
+                                 const int32_t* block_table, int block_table_stride,
+                                 const int32_t* seq_lens, int max_seq_len, float softmax_scale,
+                                 int num_splits, const int8_t* signs, const float* centroids,
+                                 void* out, int out_dtype, float* lse, void* workspace,
+                                 size_t workspace_bytes, float v_threshold, void* stream);
+
 /* tq_decode_attention without a caller-supplied workspace.  The pages have
  * no counterpart to this entry point: it exists for callers that cannot
  * allocate device memory, for example a serving engine that gives nearly all

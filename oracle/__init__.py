@@ -84,6 +84,7 @@ def lib():
                                         ctypes.c_double])
         L.orc_decode_dense.argtypes = common + [ctypes.c_void_p] * 4
         L.orc_decode_split.argtypes = common + [ctypes.c_int] + [ctypes.c_void_p] * 4
+        L.orc_sparse_v_bound.argtypes = common + [ctypes.c_double] + [ctypes.c_void_p] * 4
     return _lib
 
 
@@ -249,3 +250,12 @@ def decode_split(preset, q, cache, block_table, seq_lens, Hk, block_size, signs_
     """Rotated-q, LUT-score, split-K + log-sum-exp merge form.  Returns (out, lse)."""
     return _decode(lib().orc_decode_split, preset, q, cache, block_table, seq_lens, Hk,
                    block_size, signs_, c32, scale, [int(num_splits)])
+
+
+def sparse_v_bound(preset, q, cache, block_table, seq_lens, Hk, block_size, signs_, c32, tau,
+                   scale=None):
+    """Per-dimension bound on how far the sparse-V output may move from the
+    dense one when rows with exp(logit - max) <= tau drop out of the value
+    sum, and the weight of those rows.  Returns (bound (B,Hq,D), mass (B,Hq))."""
+    return _decode(lib().orc_sparse_v_bound, preset, q, cache, block_table, seq_lens, Hk,
+                   block_size, signs_, c32, scale, [float(tau)])

@@ -638,3 +638,57 @@ fail:
     free(H); free(qr); free(kh); free(vh); free(codes); free(po); free(pl);
     return -2;
 }
+
+int orc_sparse_v_bound(int preset, int D, int B, int Hq, int Hk, int bs,
+                       const float* q, const uint8_t* cache, int64_t num_blocks,
+                       const int32_t* block_table, int64_t bt_stride,
+                       const int32_t* seq_lens, double scale, double tau,
+                       const int8_t* signs, const float* c32,
+                       double* bound, double* mass)
+{
+    orc_layout L;
+    if (orc_get_layout(preset, D, &L)) return -1;
+    if (Hk <= 0 || Hq % Hk) return -1;
+    const int G = Hq / Hk, S = L.slot_size_aligned;
+    for (int b = 0; b < B; ++b) {
+        const int n = seq_lens[b];
+        double* kh = (double*)malloc(sizeof(double) * ((size_t)n * D + 1));
+        double* vh = (double*)malloc(sizeof(double) * ((size_t)n * D + 1));
+        double* lg = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+        for (int h = 0; h < Hk; ++h) {
+            for (int t = 0; t < n; ++t) {
+                int64_t page = block_table[(int64_t)b * bt_stride + t / bs];
+                if (page < 0 || page >= num_blocks) { free(kh); free(vh); free(lg); return -2; }
+                orc_dequant_slot(preset, D, orc_slot_ptr(cache, page, bs, t % bs, Hk, h, S),
+                                 signs, c32, kh + (size_t)t * D, vh + (size_t)t * D);
+            }
+            for (int g = 0; g < G; ++g) {
+                const int hq = h * G + g;
+                const float* qp = q + ((int64_t)b * Hq + hq) * D;
+                double* bp = bound + ((int64_t)b * Hq + hq) * D;
+                for (int i = 0; i < D; ++i) bp[i] = 0.0;
+                mass[(int64_t)b * Hq + hq] = 0.0;
+                if (n == 0) continue;
+                double m = -INFINITY;
+                for (int t = 0; t < n; ++t) {
+                    double s = 0.0;
+                    for (int i = 0; i < D; ++i) s += (double)qp[i] * kh[(size_t)t * D + i];
+                    lg[t] = scale * s;
+                    if (lg[t] > m) m = lg[t];
+                }
+                double den = 0.0, dropped = 0.0;
+                for (int t = 0; t < n; ++t) den += exp(lg[t] - m);
+                for (int t = 0; t < n; ++t) {
+                    const double e = exp(lg[t] - m);
+                    if (e > tau) continue;
+                    dropped += e;
+                    for (int i = 0; i < D; ++i) bp[i] += e * fabs(vh[(size_t)t * D + i]);
+                }
+                for (int i = 0; i < D; ++i) bp[i] /= den;
+                mass[(int64_t)b * Hq + hq] = dropped / den;
+            }
+        }
+        free(kh); free(vh); free(lg);
+    }
+    return 0;
+}

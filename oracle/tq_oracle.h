@@ -115,6 +115,20 @@ int orc_decode_split(int preset, int D, int B, int Hq, int Hk, int bs,
                      const int8_t* signs, const float* c32,
                      double* out, double* lse);
 
+/* Sparse V ("turboquant-plus.md", feature table: attention-gated row skip
+ * of the value dequantisation): a row t may drop out of the value sum when
+ * its softmax factor exp(l_t - M) is at most tau (M = the sequence's largest
+ * logit).  The output then moves from the dense one by at most
+ *   bound[b, hq, d] = sum_{t: exp(l_t - M) <= tau} p_t |v_t,d| / sum_t p_t
+ * and mass[b, hq] = sum_{t: exp(l_t - M) <= tau} p_t / sum_t p_t is the
+ * weight of the rows that may drop.  Dense logits as orc_decode_dense. */
+int orc_sparse_v_bound(int preset, int D, int B, int Hq, int Hk, int bs,
+                       const float* q, const uint8_t* cache, int64_t num_blocks,
+                       const int32_t* block_table, int64_t bt_stride,
+                       const int32_t* seq_lens, double scale, double tau,
+                       const int8_t* signs, const float* c32,
+                       double* bound, double* mass);
+
 #ifdef __cplusplus
 }
 #endif

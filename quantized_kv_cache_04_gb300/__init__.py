@@ -10,11 +10,11 @@ from . import _lib
 from ._lib import (PRESETS, TQ_2BIT_NC, TQ_3BIT_NC, TQ_4BIT_NC, TQ_BF16, TQ_F16, TQ_F32, TQ_K3V4_NC,
                    TQ_K8V4, TQError, decode_attention, dequant, load, store, tq_build_codebook,
                    tq_decode_attention, tq_decode_kernel_kind, tq_decode_pick_splits, tq_decode_workspace_bytes,
-                   tq_dequant, tq_get_layout, tq_make_signs, tq_status_string, tq_store, tq_version)
+                   tq_decode_attention_sparse_v, tq_dequant, tq_get_layout, tq_make_signs, tq_status_string, tq_store, tq_version)
 
 __all__ = ["PRESETS", "TQ_K8V4", "TQ_4BIT_NC", "TQ_K3V4_NC", "TQ_3BIT_NC", "TQ_2BIT_NC", "TQ_F16", "TQ_BF16",
            "TQ_F32", "TQError", "TQCache", "load", "store", "decode_attention", "dequant", "tq_store",
-           "tq_decode_attention", "tq_dequant", "tq_decode_kernel_kind", "tq_get_layout", "tq_build_codebook", "tq_make_signs",
+           "tq_decode_attention", "tq_decode_attention_sparse_v", "tq_dequant", "tq_decode_kernel_kind", "tq_get_layout", "tq_build_codebook", "tq_make_signs",
            "tq_decode_workspace_bytes", "tq_decode_pick_splits", "tq_status_string", "tq_version"]
 
 SIGN_SEED = 42          # per-layer seed = 42 + 1337 * layer
@@ -62,7 +62,7 @@ class TQCache:
                 self.signs, self.centroids, key_out, value_out, stream)
 
     def decode(self, query, block_table, seq_lens, max_seq_len, out, lse, workspace,
-               num_splits=0, softmax_scale=None, stream=None):
+               num_splits=0, softmax_scale=None, stream=None, v_threshold=0.0):
         decode_attention(self.preset, query, self.cache, block_table, seq_lens, max_seq_len,
                          self.num_kv_heads, self.block_size, self.signs, self.centroids, out,
-                         lse, workspace, num_splits, softmax_scale, stream)
+                         lse, workspace, num_splits, softmax_scale, stream, v_threshold)

@@ -72,6 +72,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                       _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_sz,
                                                       _c_vp])
     L.tq_decode_kernel_kind.argtypes = [_c_int] * 4
+    L.tq_decode_attention_sparse_v.argtypes = ([_c_int] * 7 + [_c_vp, _c_vp, _c_ll, _c_vp, _c_int,
+                                                               _c_vp, _c_int, ctypes.c_float, _c_int,
+                                                               _c_vp, _c_vp, _c_vp, _c_int, _c_vp,
+                                                               _c_vp, _c_sz, ctypes.c_float, _c_vp])
     L.tq_dequant.argtypes = ([_c_int] * 5 + [_c_vp, _c_ll, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int,
                                              _c_ll, _c_ll, _c_vp])
     L.tq_status_string.argtypes = [_c_int]
@@ -148,6 +152,11 @@ def tq_decode_attention(*args) -> int:
     return load().tq_decode_attention(*args)
 
 
+def tq_decode_attention_sparse_v(*args) -> int:
+    """Raw C call; arguments exactly as in include/tq.h.  Returns the status."""
+    return load().tq_decode_attention_sparse_v(*args)
+
+
 def tq_dequant(*args) -> int:
     """Raw C call; arguments exactly as in include/tq.h.  Returns the status."""
     return load().tq_dequant(*args)
@@ -199,18 +208,25 @@ def dequant(preset: int, slot_mapping, kv_cache, num_kv_heads: int, block_size: 
 
 def decode_attention(preset: int, query, kv_cache, block_table, seq_lens, max_seq_len: int,
                      num_kv_heads: int, block_size: int, signs, centroids, out, lse, workspace,
-                     num_splits: int = 0, softmax_scale: float | None = None, stream=None) -> None:
-    """tq_decode_attention on torch tensors.  query (B, Hq, D) contiguous."""
+                     num_splits: int = 0, softmax_scale: float | None = None, stream=None,
+                     v_threshold: float = 0.0) -> None:
+    """tq_decode_attention (or, with v_threshold > 0, the sparse-V form) on
+    torch tensors.  query (B, Hq, D) contiguous."""
     B, Hq, D = query.shape
     assert query.is_contiguous() and out.is_contiguous()
     scale = D ** -0.5 if softmax_scale is None else float(softmax_scale)
-    rc = tq_decode_attention(int(preset), D, B, Hq, int(num_kv_heads), int(block_size),
-                             _dtype_code(query), _ptr(query), _ptr(kv_cache), kv_cache.shape[0],
-                             _ptr(block_table), block_table.stride(0), _ptr(seq_lens),
-                             int(max_seq_len), scale, int(num_splits), _ptr(signs),
-                             _ptr(centroids), _ptr(out), _dtype_code(out), _ptr(lse),
-                             _ptr(workspace), workspace.numel() * workspace.element_size(),
-                             _stream_ptr(stream))
+    args = (int(preset), D, B, Hq, int(num_kv_heads), int(block_size),
+            _dtype_code(query), _ptr(query), _ptr(kv_cache), kv_cache.shape[0],
+            _ptr(block_table), block_table.stride(0), _ptr(seq_lens),
+            int(max_seq_len), scale, int(num_splits), _ptr(signs),
+            _ptr(centroids), _ptr(out), _dtype_code(out), _ptr(lse),
+            _ptr(workspace), workspace.numel() * workspace.element_size())
+    if v_threshold:
+        rc = tq_decode_attention_sparse_v(*args, float(v_threshold), _stream_ptr(stream))
+        if rc:
+            raise TQError("tq_decode_attention_sparse_v", rc)
+        return
+    rc = tq_decode_attention(*args, _stream_ptr(stream))
     if rc:
         raise TQError("tq_decode_attention", rc)
 

@@ -39,6 +39,7 @@ struct DecodeArgs {
     void* out;
     float* lse;
     int B, Hq, Hk, G, bs;
+    float vthr;          // sparse V: rows with p <= vthr skip the value sum (0: off)
     SlotGeom g;
 };
 
@@ -166,23 +167,34 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
         for (int g = 0; g < GM; ++g)
             s[g] = warp_sum(qv[g][0] * kv[0] + qv[g][1] * kv[1] + qv[g][2] * kv[2] + qv[g][3] * kv[3]) * knorm;
 
-        int vc[4];
-        load_codes<VBITS>(sp + a.g.off_v_data, lane, vc);
-        const float vs = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_scale)));
-        const float vz = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_zero)));
-        float vv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) vv[i] = float(vc[i]) * vs + vz;
-
+        // online softmax; sparse V: a row whose p is at most vthr keeps its
+        // weight in l but adds nothing to the value sum, and the value codes
+        // are not read when no head keeps the row (s is warp-uniform)
+        float al[GM], pv[GM];
+        bool anyv = false;
 #pragma unroll
         for (int g = 0; g < GM; ++g) {
             const float mn = fmaxf(m[g], s[g]);
-            const float al = expf(m[g] - mn), p = expf(s[g] - mn);
-            l[g] = l[g] * al + p;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[g][i] = acc[g][i] * al + p * vv[i];
+            const float p = expf(s[g] - mn);
+            al[g] = expf(m[g] - mn);
+            l[g] = l[g] * al[g] + p;
             m[g] = mn;
+            pv[g] = p > a.vthr ? p : 0.f;
+            anyv |= g < G && pv[g] > 0.f;
         }
+        float vv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (anyv) {
+            int vc[4];
+            load_codes<VBITS>(sp + a.g.off_v_data, lane, vc);
+            const float vs = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_scale)));
+            const float vz = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_zero)));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vv[i] = float(vc[i]) * vs + vz;
+        }
+#pragma unroll
+        for (int g = 0; g < GM; ++g)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[g][i] = acc[g][i] * al[g] + pv[g] * vv[i];
     }
 
     // merge the four warps' partials
@@ -405,15 +417,15 @@ int pick_splits(const tq_layout& L, int batch, int num_q_heads, int num_kv_heads
 
 }  // namespace tq
 
-extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,
-                                   int num_kv_heads, int block_size, int q_dtype, const void* query,
-                                   const uint8_t* kv_cache, long long num_blocks,
-                                   const int32_t* block_table, int block_table_stride,
-                                   const int32_t* seq_lens, int max_seq_len,
-                                   float softmax_scale, int num_splits,
-                                   const int8_t* signs, const float* centroids,
-                                   void* out, int out_dtype, float* lse,
-                                   void* workspace, size_t workspace_bytes, void* stream)
+extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch, int num_q_heads,
+                                            int num_kv_heads, int block_size, int q_dtype,
+                                            const void* query, const uint8_t* kv_cache,
+                                            long long num_blocks, const int32_t* block_table,
+                                            int block_table_stride, const int32_t* seq_lens,
+                                            int max_seq_len, float softmax_scale, int num_splits,
+                                            const int8_t* signs, const float* centroids, void* out,
+                                            int out_dtype, float* lse, void* workspace,
+                                            size_t workspace_bytes, float v_threshold, void* stream)
 {
     using namespace tq;
     tq_layout L;
@@ -424,7 +436,7 @@ extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_
         return TQ_ERR_UNSUPPORTED;
     if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads ||
         num_blocks < 0 || block_table_stride < 0 || max_seq_len < 0 || num_splits < 0 ||
-        num_splits > TQ_MAX_SPLITS)
+        num_splits > TQ_MAX_SPLITS || !(v_threshold >= 0.f && v_threshold < 1.f))
         return TQ_ERR_INVALID_ARG;
     if (num_q_heads / num_kv_heads > kMaxGroup) return TQ_ERR_UNSUPPORTED;
     if (batch == 0) return TQ_OK;
@@ -455,13 +467,14 @@ extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_
     a.Hk = num_kv_heads;
     a.G = num_q_heads / num_kv_heads;
     a.bs = block_size;
+    a.vthr = v_threshold;
     a.g = geom_of(L);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (mma_stage1_supported(L, num_kv_heads, a.G)) {
         rc = launch_mma_stage1(L, q_dtype, query, kv_cache, block_table, block_table_stride, seq_lens,
                                softmax_scale, S, signs, centroids, a.mid, batch, num_q_heads,
-                               num_kv_heads, block_size, st);
+                               num_kv_heads, block_size, v_threshold, st);
         if (rc) return rc;
     } else {
         cudaError_t e = q_dtype == TQ_F16 ? launch_stage1<__half>(preset, a, st)
@@ -472,6 +485,23 @@ extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_
                            : out_dtype == TQ_F16 ? launch_stage2<__half>(a, st)
                                                  : launch_stage2<__nv_bfloat16>(a, st);
     return e2 == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,
+                                   int num_kv_heads, int block_size, int q_dtype, const void* query,
+                                   const uint8_t* kv_cache, long long num_blocks,
+                                   const int32_t* block_table, int block_table_stride,
+                                   const int32_t* seq_lens, int max_seq_len,
+                                   float softmax_scale, int num_splits,
+                                   const int8_t* signs, const float* centroids,
+                                   void* out, int out_dtype, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream)
+{
+    return tq_decode_attention_sparse_v(preset, head_dim, batch, num_q_heads, num_kv_heads, block_size,
+                                        q_dtype, query, kv_cache, num_blocks, block_table,
+                                        block_table_stride, seq_lens, max_seq_len, softmax_scale,
+                                        num_splits, signs, centroids, out, out_dtype, lse, workspace,
+                                        workspace_bytes, 0.f, stream);
 }
 
 extern "C" int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, int num_kv_heads)

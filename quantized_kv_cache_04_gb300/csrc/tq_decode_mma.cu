@@ -51,6 +51,7 @@ struct MmaArgs {
     int copy_bytes;          // hpc * slot: the part of a token row one CTA copies
     int smem_row;            // copy_bytes padded to 16 mod 32 bytes
     int nstages;
+    float vthr;              // sparse V: rows with p <= vthr skip the value sum (0: off)
     SlotGeom g;
 };
 
@@ -701,7 +702,12 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
                 }
             }
         }
+        // Sparse V: a row whose p (against the running reference max, never
+        // above the final max) is at most vthr keeps its softmax weight in l
+        // but adds nothing to the value sum; a 16-row tile with no such row
+        // left skips its value MMAs.  vthr = 0 keeps every row with p > 0.
         float pp[2][NH][2];   // [row tile][head][row]: P' = p * v_scale
+        bool vlive[2] = {false, false};
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
             float lsum = 0.f, zsum = 0.f;
@@ -711,8 +717,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
                 for (int r = 0; r < 2; ++r) {
                     const float p = fast_exp2(s[j][rt][r] - m_run[j]);   // 0 for masked rows
                     lsum += p;
-                    zsum += ok[rt][r] ? p * vz[rt][r] : 0.f;
-                    pp[rt][j][r] = ok[rt][r] ? p * vs[rt][r] : 0.f;
+                    const bool keep = ok[rt][r] && p > a.vthr;
+                    vlive[rt] |= keep;
+                    zsum += keep ? p * vz[rt][r] : 0.f;
+                    pp[rt][j][r] = keep ? p * vs[rt][r] : 0.f;
                 }
             l_run[j] += lsum;
             z_run[j] += zsum;
@@ -721,6 +729,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         // ---- values
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt) {
+            if (a.vthr > 0.f && !__any_sync(0xffffffffu, vlive[rt])) continue;   // warp-uniform
             uint32_t pb[2][2];
             p_to_b<G>(pp[rt], gid, tig, pb);
             pv_tile<VBITS, G, KMODE == 8>(st + 16 * rt * rs + a.g.off_v_data, rs, gid, tig, vmis, pb, acc);
@@ -906,9 +915,10 @@ int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const 
                       const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
-                      cudaStream_t st)
+                      float v_threshold, cudaStream_t st)
 {
     MmaArgs a;
+    a.vthr = v_threshold;
     a.query = query;
     a.cache = kv_cache;
     a.block_table = block_table;

@@ -55,6 +55,6 @@ int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const 
                       const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
-                      cudaStream_t st);
+                      float v_threshold, cudaStream_t st);
 
 }  // namespace tq

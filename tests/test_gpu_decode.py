@@ -6,14 +6,14 @@ import pytest
 import torch
 
 import quantized_kv_cache_04_gb300 as tq
-from _helpers import check_decode, codebook, paged_problem, to_f32
+from _helpers import LSE_ABS, OUT_MAX_ABS, check_decode, codebook, paged_problem, to_f32
 
 pytestmark = pytest.mark.gpu
 PRESETS = [0, 1, 2, 3, 4]
 
 
 def _gpu_decode(preset, q, cache_np, bt, seq_lens, Hk, bs, signs, c32, num_splits=0,
-                out_dtype=torch.float32, cache_dev=None):
+                out_dtype=torch.float32, cache_dev=None, v_threshold=0.0):
     dev = torch.device("cuda")
     B, Hq, D = q.shape
     cache = cache_dev if cache_dev is not None else torch.from_numpy(cache_np).to(dev)
@@ -29,7 +29,7 @@ def _gpu_decode(preset, q, cache_np, bt, seq_lens, Hk, bs, signs, c32, num_split
     out = torch.empty((B, Hq, D), dtype=out_dtype, device=dev)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     tq.decode_attention(preset, q.to(dev).contiguous(), cache, btd, sl, maxlen, Hk, bs, sg, cc,
-                        out, lse, ws, num_splits=num_splits)
+                        out, lse, ws, num_splits=num_splits, v_threshold=v_threshold)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
@@ -193,3 +193,36 @@ def test_continuation_prefill_as_decode_rows(orc, preset):
     assert rc == 0, tq.tq_status_string(rc)
     torch.cuda.synchronize()
     check_decode(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, f"continuation preset {preset}")
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+@pytest.mark.parametrize("G,Hk,bs", [(4, 8, 16), (8, 8, 64), (4, 2, 32)])
+def test_sparse_v_within_bound(orc, preset, G, Hk, bs):
+    """Sparse V (rows with exp(logit - running max) <= tau leave the value
+    sum): the output stays within the oracle's bound of the dense attention
+    (sum over rows with exp(logit - max) <= tau of p |v| / sum p, plus the
+    dense tolerance), the LSE is the dense one, tau = 0 is the plain decode
+    bit for bit, and rows do drop (the output moves) when the bound says
+    some may.  Keys scaled x4 make the softmax peaked."""
+    rng = np.random.default_rng(9100 + 10 * preset + Hk)
+    seq_lens = [700, 129]
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng, kscale=4.0)
+    B = len(seq_lens)
+    q = torch.from_numpy(rng.normal(size=(B, G * Hk, 128)) * 1.5).to(torch.float16)
+    sl = np.asarray(seq_lens, np.int32)
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], pb["bt"], sl, Hk, bs,
+                                    pb["signs"], pb["c32"])
+    args = (preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"], pb["c32"])
+    o0, l0 = _gpu_decode(*args)
+    o0s, l0s = _gpu_decode(*args, v_threshold=0.0)
+    assert np.array_equal(o0, o0s) and np.array_equal(l0, l0s)
+    for tau in (1e-3, 0.02):
+        bound, mass = orc.sparse_v_bound(preset, to_f32(q), pb["cache"], pb["bt"], sl, Hk, bs,
+                                         pb["signs"], pb["c32"], tau)
+        o, l = _gpu_decode(*args, v_threshold=tau)
+        err = np.abs(o.astype(np.float64) - ref_o)
+        assert np.all(err <= bound + OUT_MAX_ABS), f"tau {tau}: {(err - bound).max()}"
+        assert np.abs(l - ref_l).max() <= LSE_ABS
+        if mass.max() > 1e-6:
+            assert not np.array_equal(o, o0), f"tau {tau}: nothing dropped"
+

@@ -145,3 +145,11 @@ def test_dequant_rejected_on_host():
     assert call(vs=1028) == _lib.TQ_ERR_INVALID_ARG         # stride not a multiple of 8
     assert call(k=a + 8) == _lib.TQ_ERR_INVALID_ARG         # output not 16-byte aligned
     assert call(cache=a + 2) == _lib.TQ_ERR_INVALID_ARG     # cache not 16-byte aligned
+
+
+def test_sparse_v_threshold_checked_on_host():
+    """tq_decode_attention_sparse_v takes thresholds in [0, 1) only."""
+    for tau in (1.5, -0.1, float("nan")):
+        rc = tq.tq_decode_attention_sparse_v(1, 128, 2, 8, 2, 16, 0, 1, 1, 4, 1, 4, 1, 64, 0.1, 4,
+                                             1, 1, 1, 2, 0, 16, 1 << 30, tau, None)
+        assert rc == _lib.TQ_ERR_INVALID_ARG

@@ -116,3 +116,48 @@ def test_single_token_and_equal_keys(orc, preset):
         kh, _ = orc.dequant_slot(preset, flat[rows[0], hq // 2], s, c32)
         assert np.max(np.abs(o[0, hq] - V.mean(0))) < 1e-10
         assert abs(l[0, hq] - (kh @ q[0, hq] / np.sqrt(128) + np.log(n))) < 1e-9
+
+
+def _numpy_sparse_bound(orc, preset, q, cache, bt, seq_lens, Hk, bs, s, c32, tau):
+    """The sparse-V bound by its definition, with numpy over dequantised slots."""
+    B, Hq, D = q.shape
+    G = Hq // Hk
+    bound = np.zeros((B, Hq, D))
+    mass = np.zeros((B, Hq))
+    flat = cache.reshape(-1, Hk, cache.shape[-1])
+    for b in range(B):
+        n = seq_lens[b]
+        for hq in range(Hq):
+            h = hq // G
+            K = np.zeros((n, D)); V = np.zeros((n, D))
+            for t in range(n):
+                row = bt[b, t // bs] * bs + t % bs
+                K[t], V[t] = orc.dequant_slot(preset, flat[row, h], s, c32)
+            e = np.exp(K @ q[b, hq].astype(np.float64) / np.sqrt(D) - (K @ q[b, hq] / np.sqrt(D)).max())
+            drop = e <= tau
+            bound[b, hq] = (e[drop, None] * np.abs(V[drop])).sum(0) / e.sum()
+            mass[b, hq] = e[drop].sum() / e.sum()
+    return bound, mass
+
+
+@pytest.mark.parametrize("preset", [0, 3])
+def test_sparse_v_bound(orc, preset):
+    """orc_sparse_v_bound against its definition written with numpy; tau = 0
+    drops nothing; tau just above 1 drops every row, so the bound is the
+    weighted mean of |v|, which is >= |o| of the dense attention."""
+    rng = np.random.default_rng(4400 + preset)
+    seq_lens, Hk, bs = [40, 17], 2, 16
+    cache, bt, s, c32 = _cache(orc, preset, seq_lens, Hk, bs, rng, scale_k=3.0)
+    q = rng.normal(size=(2, 4, 128)).astype(np.float32)
+    for tau in (1e-3, 0.05):
+        bd, ms = orc.sparse_v_bound(preset, q, cache, bt, np.array(seq_lens, np.int32), Hk, bs, s,
+                                    c32, tau)
+        rb, rm = _numpy_sparse_bound(orc, preset, q, cache, bt, seq_lens, Hk, bs, s, c32, tau)
+        assert np.allclose(bd, rb, rtol=1e-9, atol=1e-12) and np.allclose(ms, rm, rtol=1e-9, atol=1e-12)
+        assert ms.max() > 0                              # keys scaled x3: some rows below tau
+    bd, ms = orc.sparse_v_bound(preset, q, cache, bt, np.array(seq_lens, np.int32), Hk, bs, s, c32, 0.0)
+    assert not bd.any() and not ms.any()
+    bd, ms = orc.sparse_v_bound(preset, q, cache, bt, np.array(seq_lens, np.int32), Hk, bs, s, c32,
+                                1.0 + 1e-12)
+    out, _ = orc.decode_dense(preset, q, cache, bt, np.array(seq_lens, np.int32), Hk, bs, s, c32)
+    assert np.allclose(ms, 1.0) and np.all(bd >= np.abs(out) - 1e-12)
