@@ -58,6 +58,24 @@ extern "C" {
  * 2-bit codes: four per byte, LSB first. */
 typedef enum { TQ_K8V4 = 0, TQ_4BIT_NC = 1, TQ_K3V4_NC = 2, TQ_3BIT_NC = 3, TQ_2BIT_NC = 4 } tq_preset;
 
+/* Byte convention inside a cache block, OR-ed into the preset argument of
+ * tq_store, tq_decode_attention(_sparse_v / _noalloc), tq_dequant and
+ * tq_decode_pick_splits (tq_get_layout accepts and ignores it).  The cache
+ * shape and the slot sizes are the same either way.
+ *   default (AoS): one combined slot per (token, kv head) as described above.
+ *   TQ_LAYOUT_SOA: a data region of block_size * num_kv_heads records
+ *     [key data][value data] (key_data_bytes + value_data_bytes each; record
+ *     (t, h) at (t * num_kv_heads + h) * data_bytes from the block start),
+ *     then a metadata region of the same number of records of little-endian
+ *     uint16 fields, [k_norm][v_scale][v_zero] for the Lloyd-Max presets and
+ *     [v_scale][v_zero] for k8v4 (record (t, h) at data region end +
+ *     (t * num_kv_heads + h) * 2 * fields).  Source: "vllm.v1.attention.
+ *     backends.turboquant_attn" API page, "do_kv_cache_update" (data region +
+ *     metadata region separated per block) and "_continuation_prefill"
+ *     (metadata field count and order); the record order inside each region
+ *     is this library's reading. */
+#define TQ_LAYOUT_SOA 0x100
+
 /* Element types of K/V/Q inputs and of the attention output. */
 typedef enum { TQ_F16 = 0, TQ_BF16 = 1, TQ_F32 = 2 } tq_dtype;
 
@@ -85,7 +103,8 @@ typedef struct {
     int off_v_data, off_v_scale, off_v_zero;
 } tq_layout;
 
-/* Fill *out with the slot layout of `preset` at `head_dim` (host only).
+/* Fill *out with the slot layout of `preset` at `head_dim` (host only; the
+ * TQ_LAYOUT_SOA bit is ignored).
  * head_dim must be a positive multiple of 8.  Returns TQ_OK or
  * TQ_ERR_INVALID_ARG / TQ_ERR_UNSUPPORTED. */
 int tq_get_layout(int preset, int head_dim, tq_layout* out);

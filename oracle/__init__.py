@@ -25,6 +25,7 @@ _HDR = os.path.join(_HERE, "tq_oracle.h")
 _OUT = os.path.join(_HERE, "_build", "liboracle.so")
 
 K8V4, TQ4_NC, K3V4_NC, TQ3_NC, TQ2_NC = 0, 1, 2, 3, 4
+LAYOUT_SOA = 0x100          # OR-ed into a preset: SoA byte convention inside cache blocks
 PRESETS = {"turboquant_k8v4": K8V4, "turboquant_4bit_nc": TQ4_NC,
            "turboquant_k3v4_nc": K3V4_NC, "turboquant_3bit_nc": TQ3_NC,
            "turboquant_2bit_nc": TQ2_NC}

@@ -27,8 +27,9 @@
 int orc_get_layout(int preset, int D, orc_layout* L)
 {
     if (!L || D <= 0) return -1;
+    if (preset & ~(0xFF | ORC_LAYOUT_SOA)) return -1;
     memset(L, 0, sizeof(*L));
-    switch (preset) {
+    switch (preset & 0xFF) {
     case ORC_K8V4:    L->key_fp8 = 1; L->key_bits = 8; L->value_bits = 4; L->norm_correction = 0; break;
     case ORC_4BIT_NC: L->key_fp8 = 0; L->key_bits = 4; L->value_bits = 4; L->norm_correction = 1; break;
     case ORC_K3V4_NC: L->key_fp8 = 0; L->key_bits = 3; L->value_bits = 4; L->norm_correction = 1; break;
@@ -408,6 +409,53 @@ int orc_store_one(int preset, int D, const float* k, const float* v,
  * num_kv_heads, slot); slot index = slot_mapping[token]; block =
  * slot // block_size, offset = slot % block_size.  Negative slots are
  * padding and are not written (the usual vLLM convention). */
+/* Where the bytes of slot (block blk, token off, head h) sit in the cache:
+ * AoS: one contiguous slot; SoA: a data record and a metadata record.  The
+ * copies below move whole slots (in their AoS byte order) in and out. */
+static void orc_soa_places(const orc_layout* L, int64_t blk, int bs, int off, int Hk, int h,
+                           int64_t* data, int64_t* meta, int* nf, int fields[3])
+{
+    const int64_t S = L->slot_size_aligned, db = L->key_data_bytes + L->value_data_bytes;
+    *nf = L->key_fp8 ? 2 : 3;
+    const int64_t rec = (int64_t)off * Hk + h, base = blk * bs * Hk * S;
+    *data = base + rec * db;
+    *meta = base + (int64_t)bs * Hk * db + rec * 2 * *nf;
+    if (L->key_fp8) { fields[0] = L->off_v_scale; fields[1] = L->off_v_zero; }
+    else { fields[0] = L->off_k_norm; fields[1] = L->off_v_scale; fields[2] = L->off_v_zero; }
+}
+
+static void orc_put_slot(int preset, const orc_layout* L, uint8_t* cache, int64_t blk, int bs,
+                         int off, int Hk, int h, const uint8_t* slot)
+{
+    const int64_t S = L->slot_size_aligned;
+    if (!(preset & ORC_LAYOUT_SOA)) {
+        memcpy(cache + ((blk * bs + off) * Hk + h) * S, slot, (size_t)S);
+        return;
+    }
+    int64_t data, meta;
+    int nf, fields[3];
+    orc_soa_places(L, blk, bs, off, Hk, h, &data, &meta, &nf, fields);
+    memcpy(cache + data, slot, (size_t)L->key_data_bytes);
+    memcpy(cache + data + L->key_data_bytes, slot + L->off_v_data, (size_t)L->value_data_bytes);
+    for (int f = 0; f < nf; ++f) memcpy(cache + meta + 2 * f, slot + fields[f], 2);
+}
+
+/* The slot's bytes in AoS order: a pointer into the cache (AoS) or `buf`. */
+static const uint8_t* orc_get_slot(int preset, const orc_layout* L, const uint8_t* cache, int64_t blk,
+                                   int bs, int off, int Hk, int h, uint8_t* buf)
+{
+    const int64_t S = L->slot_size_aligned;
+    if (!(preset & ORC_LAYOUT_SOA)) return cache + ((blk * bs + off) * Hk + h) * S;
+    int64_t data, meta;
+    int nf, fields[3];
+    orc_soa_places(L, blk, bs, off, Hk, h, &data, &meta, &nf, fields);
+    memset(buf, 0, (size_t)S);
+    memcpy(buf, cache + data, (size_t)L->key_data_bytes);
+    memcpy(buf + L->off_v_data, cache + data + L->key_data_bytes, (size_t)L->value_data_bytes);
+    for (int f = 0; f < nf; ++f) memcpy(buf + fields[f], cache + meta + 2 * f, 2);
+    return buf;
+}
+
 int orc_store(int preset, int D, int N, int Hk, int bs,
               const float* key, const float* value, const int64_t* slot_mapping,
               uint8_t* cache, int64_t num_blocks,
@@ -422,10 +470,12 @@ int orc_store(int preset, int D, int N, int Hk, int bs,
         int64_t blk = sl / bs, off = sl % bs;
         if (blk >= num_blocks) return -2;
         for (int h = 0; h < Hk; ++h) {
-            uint8_t* dst = cache + ((blk * bs + off) * Hk + h) * S;
+            uint8_t slot[1024];
             const float* kp = key + ((int64_t)t * Hk + h) * D;
             const float* vp = value + ((int64_t)t * Hk + h) * D;
-            orc_store_one(preset, D, kp, vp, signs, c32, m32, dst, NULL);
+            if (S > (int64_t)sizeof(slot)) return -1;
+            orc_store_one(preset, D, kp, vp, signs, c32, m32, slot, NULL);
+            orc_put_slot(preset, &L, cache, blk, bs, (int)off, Hk, h, slot);
         }
     }
     return 0;
@@ -479,11 +529,6 @@ int orc_dequant_slot(int preset, int D, const uint8_t* slot,
  * lse = ln sum exp(logit) (natural log, scale included).  An empty
  * sequence gives out = 0 and lse = -inf.
  * ==================================================================== */
-static const uint8_t* orc_slot_ptr(const uint8_t* cache, int64_t page, int bs, int off,
-                                   int Hk, int h, int S)
-{
-    return cache + (((int64_t)page * bs + off) * Hk + h) * (int64_t)S;
-}
 
 int orc_decode_dense(int preset, int D, int B, int Hq, int Hk, int bs,
                      const float* q, const uint8_t* cache, int64_t num_blocks,
@@ -495,7 +540,9 @@ int orc_decode_dense(int preset, int D, int B, int Hq, int Hk, int bs,
     orc_layout L;
     if (orc_get_layout(preset, D, &L)) return -1;
     if (Hk <= 0 || Hq % Hk) return -1;
-    const int G = Hq / Hk, S = L.slot_size_aligned;
+    const int G = Hq / Hk;
+    uint8_t sbuf[1024];                      /* a slot gathered from SoA records */
+    if (L.slot_size_aligned > (int)sizeof(sbuf)) return -1;
     for (int b = 0; b < B; ++b) {
         const int n = seq_lens[b];
         double* kh = (double*)malloc(sizeof(double) * ((size_t)n * D + 1));
@@ -505,7 +552,7 @@ int orc_decode_dense(int preset, int D, int B, int Hq, int Hk, int bs,
             for (int t = 0; t < n; ++t) {
                 int64_t page = block_table[(int64_t)b * bt_stride + t / bs];
                 if (page < 0 || page >= num_blocks) { free(kh); free(vh); free(lg); return -2; }
-                orc_dequant_slot(preset, D, orc_slot_ptr(cache, page, bs, t % bs, Hk, h, S),
+                orc_dequant_slot(preset, D, orc_get_slot(preset, &L, cache, page, bs, t % bs, Hk, h, sbuf),
                                  signs, c32, kh + (size_t)t * D, vh + (size_t)t * D);
             }
             for (int g = 0; g < G; ++g) {
@@ -555,7 +602,9 @@ int orc_decode_split(int preset, int D, int B, int Hq, int Hk, int bs,
     orc_layout L;
     if (orc_get_layout(preset, D, &L)) return -1;
     if (Hk <= 0 || Hq % Hk || num_splits < 1) return -1;
-    const int G = Hq / Hk, S = L.slot_size_aligned;
+    const int G = Hq / Hk;
+    uint8_t sbuf[1024];                      /* a slot gathered from SoA records */
+    if (L.slot_size_aligned > (int)sizeof(sbuf)) return -1;
     double* H = (double*)malloc(sizeof(double) * D * D);
     orc_hadamard(D, H);
     double* qr = (double*)malloc(sizeof(double) * D);
@@ -586,7 +635,7 @@ int orc_decode_split(int preset, int D, int B, int Hq, int Hk, int bs,
                 for (int t = t0; t < t1; ++t) {
                     int64_t page = block_table[(int64_t)b * bt_stride + t / bs];
                     if (page < 0 || page >= num_blocks) goto fail;
-                    const uint8_t* sp = orc_slot_ptr(cache, page, bs, t % bs, Hk, h, S);
+                    const uint8_t* sp = orc_get_slot(preset, &L, cache, page, bs, t % bs, Hk, h, sbuf);
                     double sc;
                     if (L.key_fp8) {
                         orc_dequant_slot(preset, D, sp, signs, c32, kh, NULL);
@@ -649,7 +698,9 @@ int orc_sparse_v_bound(int preset, int D, int B, int Hq, int Hk, int bs,
     orc_layout L;
     if (orc_get_layout(preset, D, &L)) return -1;
     if (Hk <= 0 || Hq % Hk) return -1;
-    const int G = Hq / Hk, S = L.slot_size_aligned;
+    const int G = Hq / Hk;
+    uint8_t sbuf[1024];                      /* a slot gathered from SoA records */
+    if (L.slot_size_aligned > (int)sizeof(sbuf)) return -1;
     for (int b = 0; b < B; ++b) {
         const int n = seq_lens[b];
         double* kh = (double*)malloc(sizeof(double) * ((size_t)n * D + 1));
@@ -659,7 +710,7 @@ int orc_sparse_v_bound(int preset, int D, int B, int Hq, int Hk, int bs,
             for (int t = 0; t < n; ++t) {
                 int64_t page = block_table[(int64_t)b * bt_stride + t / bs];
                 if (page < 0 || page >= num_blocks) { free(kh); free(vh); free(lg); return -2; }
-                orc_dequant_slot(preset, D, orc_slot_ptr(cache, page, bs, t % bs, Hk, h, S),
+                orc_dequant_slot(preset, D, orc_get_slot(preset, &L, cache, page, bs, t % bs, Hk, h, sbuf),
                                  signs, c32, kh + (size_t)t * D, vh + (size_t)t * D);
             }
             for (int g = 0; g < G; ++g) {

@@ -33,6 +33,12 @@ extern "C" {
 #define ORC_K3V4_NC 2
 #define ORC_3BIT_NC 3
 #define ORC_2BIT_NC 4   /* Turbo2: 2-bit Lloyd-Max keys + norm correction, 2-bit values */
+/* OR-ed into a preset: the SoA byte convention inside each cache block (a
+ * data region of [key data][value data] records, then a metadata region of
+ * uint16 [k_norm][v_scale][v_zero] records, [v_scale][v_zero] for FP8 keys;
+ * record (t, h) at index t * Hk + h of each region).  Slot bytes are the
+ * same; only where they sit in the block changes. */
+#define ORC_LAYOUT_SOA 0x100
 
 /* Slot layout derived from [vLLM-API] "__init__" (mse bytes / value data
  * bytes formulas) and [vLLM-API] "_continuation_prefill" (field order

@@ -7,12 +7,12 @@ cache; `_lib` holds the raw C-ABI binding.
 from __future__ import annotations
 
 from . import _lib
-from ._lib import (PRESETS, TQ_2BIT_NC, TQ_3BIT_NC, TQ_4BIT_NC, TQ_BF16, TQ_F16, TQ_F32, TQ_K3V4_NC,
+from ._lib import (PRESETS, TQ_2BIT_NC, TQ_3BIT_NC, TQ_4BIT_NC, TQ_LAYOUT_SOA, TQ_BF16, TQ_F16, TQ_F32, TQ_K3V4_NC,
                    TQ_K8V4, TQError, decode_attention, dequant, load, store, tq_build_codebook,
                    tq_decode_attention, tq_decode_kernel_kind, tq_decode_pick_splits, tq_decode_workspace_bytes,
                    tq_decode_attention_sparse_v, tq_dequant, tq_get_layout, tq_make_signs, tq_status_string, tq_store, tq_version)
 
-__all__ = ["PRESETS", "TQ_K8V4", "TQ_4BIT_NC", "TQ_K3V4_NC", "TQ_3BIT_NC", "TQ_2BIT_NC", "TQ_F16", "TQ_BF16",
+__all__ = ["PRESETS", "TQ_K8V4", "TQ_4BIT_NC", "TQ_K3V4_NC", "TQ_3BIT_NC", "TQ_2BIT_NC", "TQ_LAYOUT_SOA", "TQ_F16", "TQ_BF16",
            "TQ_F32", "TQError", "TQCache", "load", "store", "decode_attention", "dequant", "tq_store",
            "tq_decode_attention", "tq_decode_attention_sparse_v", "tq_dequant", "tq_decode_kernel_kind", "tq_get_layout", "tq_build_codebook", "tq_make_signs",
            "tq_decode_workspace_bytes", "tq_decode_pick_splits", "tq_status_string", "tq_version"]

@@ -15,6 +15,7 @@ from . import build as _build
 
 TQ_K8V4, TQ_4BIT_NC, TQ_K3V4_NC, TQ_3BIT_NC, TQ_2BIT_NC = 0, 1, 2, 3, 4
 TQ_F16, TQ_BF16, TQ_F32 = 0, 1, 2
+TQ_LAYOUT_SOA = 0x100       # OR-ed into a preset: SoA byte convention inside cache blocks
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA = 0, -1, -2, -3, -4
 TQ_MAX_SPLITS = 256
 PRESETS = {"turboquant_k8v4": TQ_K8V4, "turboquant_4bit_nc": TQ_4BIT_NC,

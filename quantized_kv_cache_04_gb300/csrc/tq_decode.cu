@@ -141,11 +141,11 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
         for (int i = 0; i < 4; ++i) acc[g][i] = 0.f;
     }
 
-    const int SB = a.g.slot;
     const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
     for (int t = t0 + warp; t < t1; t += kWarps) {
         const long long page = bt[t / a.bs];
-        const uint8_t* sp = a.cache + ((page * a.bs + t % a.bs) * a.Hk + h) * (long long)SB;
+        const uint8_t *sp, *mp;              // data and metadata of the record
+        slot_ptrs(a.g, a.cache, page, t % a.bs, h, a.bs, a.Hk, sp, mp);
 
         float kv[4];
         float knorm = 1.f;
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
             load_codes<KBITS>(sp, lane, c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) kv[i] = s_cent[c[i]];
-            knorm = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_k_norm)));
+            knorm = __half2float(__ushort_as_half(ld_u16(mp + a.g.m_norm)));
         }
         float s[GM];
 #pragma unroll
@@ -185,9 +185,9 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
         float vv[4] = {0.f, 0.f, 0.f, 0.f};
         if (anyv) {
             int vc[4];
-            load_codes<VBITS>(sp + a.g.off_v_data, lane, vc);
-            const float vs = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_scale)));
-            const float vz = __half2float(__ushort_as_half(ld_u16(sp + a.g.off_v_zero)));
+            load_codes<VBITS>(sp + a.g.v_off, lane, vc);
+            const float vs = __half2float(__ushort_as_half(ld_u16(mp + a.g.m_scale)));
+            const float vz = __half2float(__ushort_as_half(ld_u16(mp + a.g.m_zero)));
 #pragma unroll
             for (int i = 0; i < 4; ++i) vv[i] = float(vc[i]) * vs + vz;
         }
@@ -319,7 +319,7 @@ cudaError_t launch_stage1_g(const DecodeArgs& a, cudaStream_t st)
 template <typename TQ>
 cudaError_t launch_stage1(int preset, const DecodeArgs& a, cudaStream_t st)
 {
-    switch (preset) {
+    switch (preset & 0xFF) {
     case TQ_K8V4:    return launch_stage1_g<TQ, true, 4, 4>(a, st);
     case TQ_4BIT_NC: return launch_stage1_g<TQ, false, 4, 4>(a, st);
     case TQ_K3V4_NC: return launch_stage1_g<TQ, false, 3, 4>(a, st);
@@ -344,9 +344,9 @@ int v1_slots(int G, int num_sms)
 
 // (CTAs per split, resident CTA slots) of the stage-1 kernel for a shape,
 // cached per device.
-void stage1_shape(const tq_layout& L, int Hk, int G, int* cps, int* slots)
+void stage1_shape(const tq_layout& L, bool soa, int Hk, int G, int* cps, int* slots)
 {
-    struct Entry { int dev, kf8, kb, vb, hk, g, cps, slots; };
+    struct Entry { int dev, kf8, kb, vb, soa, hk, g, cps, slots; };
     static std::mutex mu;
     static std::vector<Entry> cache;
     int dev = -1, num_sms = 0;
@@ -360,15 +360,15 @@ void stage1_shape(const tq_layout& L, int Hk, int G, int* cps, int* slots)
         std::lock_guard<std::mutex> lock(mu);
         for (const Entry& e : cache)
             if (e.dev == dev && e.kf8 == L.key_fp8 && e.kb == L.key_bits && e.vb == L.value_bits &&
-                e.hk == Hk && e.g == G) {
+                e.soa == int(soa) && e.hk == Hk && e.g == G) {
                 *cps = e.cps;
                 *slots = e.slots;
                 return;
             }
     }
     int c = Hk, n = 0;
-    if (mma_stage1_supported(L, Hk, G)) {
-        mma_stage1_shape(L, Hk, G, num_sms, &c, &n);
+    if (mma_stage1_supported(L, soa, Hk, G)) {
+        mma_stage1_shape(L, soa, Hk, G, num_sms, &c, &n);
     } else if (num_sms > 0) {
         c = Hk;                    // grid (splits, kv heads, batch)
         if (L.key_fp8) n = v1_slots<true, 4, 4>(G, num_sms);
@@ -382,18 +382,18 @@ void stage1_shape(const tq_layout& L, int Hk, int G, int* cps, int* slots)
         n = 2 * kNumSMs;           // no device to ask: two CTAs per SM of a GB300
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (cache.size() < 256) cache.push_back({dev, L.key_fp8, L.key_bits, L.value_bits, Hk, G, c, n});
+    if (cache.size() < 256) cache.push_back({dev, L.key_fp8, L.key_bits, L.value_bits, int(soa), Hk, G, c, n});
     *cps = c;
     *slots = n;
 }
 
 }  // namespace
 
-int pick_splits(const tq_layout& L, int batch, int num_q_heads, int num_kv_heads, int max_seq_len)
+int pick_splits(const tq_layout& L, bool soa, int batch, int num_q_heads, int num_kv_heads, int max_seq_len)
 {
     if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_seq_len <= 0) return 1;
     int cps = 1, slots = 1;
-    stage1_shape(L, num_kv_heads, num_q_heads / num_kv_heads, &cps, &slots);
+    stage1_shape(L, soa, num_kv_heads, num_q_heads / num_kv_heads, &cps, &slots);
     // Critical path of stage 1 in 32-token tiles: the CTAs of all splits run
     // in ceil(CTAs / slots) waves, each as long as one split's tiles plus a
     // fixed start-up (q preparation, first copy latency, epilogue) worth about
@@ -444,7 +444,8 @@ extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch,
         return TQ_ERR_INVALID_ARG;
     if (!L.key_fp8 && (!signs || !centroids)) return TQ_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) & 15) return TQ_ERR_INVALID_ARG;
-    const int S = num_splits ? num_splits : pick_splits(L, batch, num_q_heads, num_kv_heads, max_seq_len);
+    const bool soa = is_soa(preset);
+    const int S = num_splits ? num_splits : pick_splits(L, soa, batch, num_q_heads, num_kv_heads, max_seq_len);
     if (workspace_bytes < tq_decode_workspace_bytes(batch, num_q_heads, S, head_dim))
         return TQ_ERR_WORKSPACE;
 
@@ -468,11 +469,11 @@ extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch,
     a.G = num_q_heads / num_kv_heads;
     a.bs = block_size;
     a.vthr = v_threshold;
-    a.g = geom_of(L);
+    a.g = geom_of(L, soa);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    if (mma_stage1_supported(L, num_kv_heads, a.G)) {
-        rc = launch_mma_stage1(L, q_dtype, query, kv_cache, block_table, block_table_stride, seq_lens,
+    if (mma_stage1_supported(L, soa, num_kv_heads, a.G)) {
+        rc = launch_mma_stage1(L, soa, q_dtype, query, kv_cache, block_table, block_table_stride, seq_lens,
                                softmax_scale, S, signs, centroids, a.mid, batch, num_q_heads,
                                num_kv_heads, block_size, v_threshold, st);
         if (rc) return rc;
@@ -511,5 +512,5 @@ extern "C" int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, 
     if (fill_layout(preset, head_dim, &L) || head_dim != kHeadDim || num_kv_heads < 1 ||
         num_q_heads < 1 || num_q_heads % num_kv_heads)
         return -1;
-    return mma_stage1_supported(L, num_kv_heads, num_q_heads / num_kv_heads) ? 1 : 0;
+    return mma_stage1_supported(L, is_soa(preset), num_kv_heads, num_q_heads / num_kv_heads) ? 1 : 0;
 }

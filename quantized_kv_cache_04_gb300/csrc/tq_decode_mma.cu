@@ -48,8 +48,9 @@ struct MmaArgs {
     int Hq, Hk, G, bs, bs_log2;
     int row_bytes;           // global token row: Hk * slot
     int hpc;                 // kv heads per CTA (Hk, or 4 for FP8 keys)
-    int copy_bytes;          // hpc * slot: the part of a token row one CTA copies
+    int copy_bytes;          // AoS: hpc * slot; SoA: hpc * data record (the data part a CTA copies)
     int smem_row;            // copy_bytes padded to 16 mod 32 bytes
+    int meta_bytes;          // SoA: hpc * metadata record per token (0 for AoS)
     int nstages;
     float vthr;              // sparse V: rows with p <= vthr skip the value sum (0: off)
     SlotGeom g;
@@ -469,9 +470,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // and the shared row stride equals the global one, else one copy per row
     // (issued by the 32 lanes of one warp).
     const int row_bytes = a.row_bytes;        // global token row (Hk slots)
-    const int cb = a.copy_bytes;              // bytes of it this CTA copies
+    const int cb = a.copy_bytes;              // bytes of it this CTA copies (SoA: data part)
     const int rs = a.smem_row;                // shared row stride: 16 mod 32 bytes
-    const int stage_bytes = kTile * rs;
+    const int mb = a.meta_bytes;              // SoA: metadata part per token, rows after the data rows
+    const int stage_bytes = kTile * (rs + mb);
     const int NST = a.nstages;
     const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
     const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
@@ -490,26 +492,39 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // Only rows of tokens < L are copied: block-table entries past the
     // sequence's last page are never read.  Skipped rows keep stale bytes and
     // are masked out of the softmax.
+    // SoA blocks: the token rows' data parts and metadata parts lie in two
+    // regions of the block; each row (or page segment) takes one copy per
+    // region, the metadata landing in rows of mb bytes after the data rows.
+    const int soa = a.g.soa;
+    const long long hs_g = soa ? a.g.data_bytes : a.g.slot;    // head stride in a global data row
+    const long long drow = soa ? (long long)a.Hk * a.g.data_bytes : row_bytes;
     auto issue = [&](int tile, int stage) {   // called by all lanes of one warp
         if (tile >= ntiles) return;
         uint8_t* dst = smem + stage * stage_bytes;
         uint64_t* bar = &full[stage];
         const int tbase = t_begin + tile * kTile;
-        const bool per_segment = rs == row_bytes && cb == row_bytes;
-        const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile
+        const bool per_segment = rs == drow && cb == drow && (!soa || mb == a.Hk * a.g.meta_bytes);
+        const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile and region
         const int seg_len = per_segment ? seg_rows : 1;               // rows per copy
         const int nlive = min(nseg, (L - tbase + seg_len - 1) / seg_len);
         if (lane == 0) {
             fence_async_shared();             // prior generic reads of this stage before the async writes
-            mbar_expect_tx(bar, uint32_t(nlive * seg_len * cb));
+            mbar_expect_tx(bar, uint32_t(nlive * seg_len * (cb + mb)));
         }
         __syncwarp();
         if (lane < nlive) {
             const int t = tbase + lane * seg_len;
             const long long page = bt[t >> lg];
-            const uint8_t* src = a.cache + ((page << lg) + (t & ((1 << lg) - 1))) * (long long)row_bytes +
-                                 h0 * a.g.slot;
-            bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * cb), bar);
+            const int off = t & ((1 << lg) - 1);
+            if (soa) {
+                const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
+                bulk_g2s(dst + lane * seg_len * rs, blk + off * drow + h0 * hs_g, uint32_t(seg_len * cb), bar);
+                const uint8_t* meta = blk + (1LL << lg) * drow + ((long long)off * a.Hk + h0) * a.g.meta_bytes;
+                bulk_g2s(dst + kTile * rs + lane * seg_len * mb, meta, uint32_t(seg_len * mb), bar);
+            } else {
+                const uint8_t* src = a.cache + ((page << lg) + off) * (long long)row_bytes + h0 * hs_g;
+                bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * cb), bar);
+            }
         }
     };
     // The q staging area (hpc x (4 or 8) heads x 512 B) sits at the end of the
@@ -622,13 +637,17 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
     const int tau0 = qk_token(gid), tau1 = qk_token(gid + 8);
-    const int hoff = warp * a.g.slot;          // this warp's slot in a shared row
+    const int hoff = warp * int(hs_g);         // this warp's slot (SoA: data record) in a shared row
     const int kmis = hoff & 2;
-    const int vmis = (hoff + a.g.off_v_data) & 2;
+    const int vmis = (hoff + a.g.v_off) & 2;
+    // metadata rows: AoS = the data rows (fields inside the slot); SoA = the
+    // rows after the data rows, mb bytes each
+    const int mrs = soa ? mb : rs;
+    const int moff = soa ? kTile * rs + warp * a.g.meta_bytes : hoff;
 
     // One 32-token tile in stage memory st (this warp's slot at offset 0).
     // PARTIAL: some of its tokens lie at or past t_end and are masked.
-    auto tile = [&](const uint8_t* st, int t0, auto partial_tag) {
+    auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag) {
         constexpr bool PARTIAL = decltype(partial_tag)::value;
         // ---- scores of both 16-row tiles
         float s[NH][2][2], vs[2][2], vz[2][2];
@@ -637,14 +656,16 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         for (int rt = 0; rt < 2; ++rt) {
             const uint8_t* r0 = st + (16 * rt + tau0) * rs;
             const uint8_t* r1 = st + (16 * rt + tau1) * rs;
+            const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
+            const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
             qk_tile<KMODE, G>(r0, r1, tig, kmis, bq, bql, T, sc, scl);
             float n0 = 1.f, n1 = 1.f;
-            if constexpr (KMODE != 8) { n0 = lds_f16(r0 + a.g.off_k_norm); n1 = lds_f16(r1 + a.g.off_k_norm); }
-            vs[rt][0] = lds_f16(r0 + a.g.off_v_scale);
-            vz[rt][0] = lds_f16(r0 + a.g.off_v_zero);
-            vs[rt][1] = lds_f16(r1 + a.g.off_v_scale);
-            vz[rt][1] = lds_f16(r1 + a.g.off_v_zero);
+            if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
+            vs[rt][0] = lds_f16(m0 + a.g.m_scale);
+            vz[rt][0] = lds_f16(m0 + a.g.m_zero);
+            vs[rt][1] = lds_f16(m1 + a.g.m_scale);
+            vz[rt][1] = lds_f16(m1 + a.g.m_zero);
             ok[rt][0] = !PARTIAL || t0 + 16 * rt + tau0 < t_end;
             ok[rt][1] = !PARTIAL || t0 + 16 * rt + tau1 < t_end;
             if constexpr (G == 4) {
@@ -732,7 +753,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             if (a.vthr > 0.f && !__any_sync(0xffffffffu, vlive[rt])) continue;   // warp-uniform
             uint32_t pb[2][2];
             p_to_b<G>(pp[rt], gid, tig, pb);
-            pv_tile<VBITS, G, KMODE == 8>(st + 16 * rt * rs + a.g.off_v_data, rs, gid, tig, vmis, pb, acc);
+            pv_tile<VBITS, G, KMODE == 8>(st + 16 * rt * rs + a.g.v_off, rs, gid, tig, vmis, pb, acc);
         }
     };
 
@@ -745,9 +766,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         const bool ok_wait = mbar_wait(&full[stage], parity, kWaitLimit);
         if (!__all_sync(0xffffffffu, ok_wait)) { failed_at = it; break; }
         const uint8_t* st = smem + stage * stage_bytes + hoff;
+        const uint8_t* sm = smem + stage * stage_bytes + moff;
         const int t0 = t_begin + it * kTile;
-        if (t0 + kTile <= t_end) tile(st, t0, std::false_type{});
-        else                     tile(st, t0, std::true_type{});
+        if (t0 + kTile <= t_end) tile(st, sm, t0, std::false_type{});
+        else                     tile(st, sm, t0, std::true_type{});
 
         // ---- this warp is done with the stage; the last warp refills it
         __syncwarp();
@@ -836,22 +858,26 @@ cudaError_t launch_q(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
 
 // Launch geometry shared by the launcher and the occupancy query.
 struct MmaGeom {
-    int hpc, copy_bytes, smem_row, nstages;
+    int hpc, copy_bytes, smem_row, meta_bytes, nstages;
     size_t smem;
 };
 
-MmaGeom mma_geom(const tq_layout& L, int Hk, int G)
+MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G)
 {
     MmaGeom m;
-    // FP8-key rows split into CTAs of 4 kv heads (4 x 196 B is a whole number
+    const SlotGeom g = geom_of(L, soa);
+    const int rec = soa ? g.data_bytes : L.slot_size_aligned;   // data bytes per (token, head)
+    // FP8-key rows split into CTAs of 4 kv heads (4 records are a whole number
     // of 16-byte copy units): half-size CTAs, four per SM, each waiting on
     // only 4 warps before a stage is refilled
-    m.hpc = (L.key_fp8 && Hk % 4 == 0 && Hk > 4 && (4 * L.slot_size_aligned) % 16 == 0) ? 4 : Hk;
-    m.copy_bytes = m.hpc * L.slot_size_aligned;
+    m.hpc = (L.key_fp8 && Hk % 4 == 0 && Hk > 4 && (4 * rec) % 16 == 0 && (!soa || (4 * g.meta_bytes) % 16 == 0))
+                ? 4 : Hk;
+    m.copy_bytes = m.hpc * rec;
+    m.meta_bytes = soa ? m.hpc * g.meta_bytes : 0;
     // a shared row stride of 16 mod 32 bytes (4 mod 8 words) puts the rows a
     // warp reads in the same instruction on distinct bank quads
     m.smem_row = (m.copy_bytes % 32 == 0) ? m.copy_bytes + 16 : m.copy_bytes;
-    const int stage = kTile * m.smem_row;
+    const int stage = kTile * (m.smem_row + m.meta_bytes);
     // ring budget: two CTAs of Hk warps, or four CTAs of 4 warps, per SM
     int nst = (m.hpc < Hk ? 56 * 1024 : 100 * 1024) / stage;
     nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
@@ -876,22 +902,23 @@ int slots_t(const MmaGeom& m, int num_sms)
 
 }  // namespace
 
-bool mma_stage1_supported(const tq_layout& L, int num_kv_heads, int group)
+bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int group)
 {
     const bool keys_ok = (L.key_fp8 && L.value_bits == 4) ||
                          (!L.key_fp8 && (L.key_bits == 3 || (L.key_bits == 4 && L.value_bits == 4) ||
                                          (L.key_bits == 2 && L.value_bits == 2)));
     const bool vals_ok = L.value_bits >= 2 && L.value_bits <= 4;
     if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > 8) return false;
-    const MmaGeom m = mma_geom(L, num_kv_heads, group);
+    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
     const int row = m.copy_bytes;
-    return m.hpc <= 16 && row % 16 == 0 && 2 * kTile * (row + 16) <= 110 * 1024;
+    return m.hpc <= 16 && row % 16 == 0 && m.meta_bytes % 16 == 0 &&
+           2 * kTile * (row + 16 + m.meta_bytes) <= 110 * 1024;
 }
 
-void mma_stage1_shape(const tq_layout& L, int num_kv_heads, int group, int num_sms, int* ctas_per_split,
-                      int* slots)
+void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int num_sms,
+                      int* ctas_per_split, int* slots)
 {
-    const MmaGeom m = mma_geom(L, num_kv_heads, group);
+    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
     *ctas_per_split = num_kv_heads / m.hpc;
     int n = 0;
     if (num_sms > 0) {
@@ -911,7 +938,7 @@ void mma_stage1_shape(const tq_layout& L, int num_kv_heads, int group, int num_s
     *slots = n;
 }
 
-int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const uint8_t* kv_cache,
+int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* query, const uint8_t* kv_cache,
                       const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
@@ -935,12 +962,13 @@ int launch_mma_stage1(const tq_layout& L, int q_dtype, const void* query, const 
     a.bs = bs;
     a.bs_log2 = bs == 16 ? 4 : bs == 32 ? 5 : bs == 64 ? 6 : 7;
     a.row_bytes = Hk * L.slot_size_aligned;
-    const MmaGeom m = mma_geom(L, Hk, a.G);
+    const MmaGeom m = mma_geom(L, soa, Hk, a.G);
     a.hpc = m.hpc;
     a.copy_bytes = m.copy_bytes;
     a.smem_row = m.smem_row;
+    a.meta_bytes = m.meta_bytes;
     a.nstages = m.nstages;
-    a.g = geom_of(L);
+    a.g = geom_of(L, soa);
     cudaError_t e = q_dtype == TQ_F16 ? launch_q<__half>(a, B, m.smem, st)
                                       : launch_q<__nv_bfloat16>(a, B, m.smem, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

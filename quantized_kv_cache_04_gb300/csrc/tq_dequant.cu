@@ -20,7 +20,7 @@ namespace {
 struct DqArgs {
     const uint8_t* cache;
     long long nslots;                 // num_blocks * block_size
-    int Hk, num_tokens;
+    int Hk, num_tokens, bs;
     const int64_t* slot_mapping;
     const int8_t* signs;
     const float* centroids;
@@ -108,18 +108,21 @@ struct PairRaw {
     uint16_t norm, scale, zero;
 };
 
+// s: the record's data (key data at 0, value data at v_off); m: its metadata
+// (the slot itself for AoS).
 template <int KBITS, int VBITS>
-__device__ __forceinline__ void load_pair(const DqArgs& a, const uint8_t* s, int lane, PairRaw<KBITS, VBITS>& r)
+__device__ __forceinline__ void load_pair(const DqArgs& a, const uint8_t* s, const uint8_t* m, int lane,
+                                          PairRaw<KBITS, VBITS>& r)
 {
     if constexpr (KBITS == 0) {
-        r.kw = *reinterpret_cast<const uint32_t*>(s + 4 * lane);   // slot 196: 4-byte aligned
+        r.kw = *reinterpret_cast<const uint32_t*>(s + 4 * lane);   // slot 196 / record 192: 4-byte aligned
     } else {
         load_codes<KBITS>(s, lane, r.kc);
-        r.norm = ld_u16(s + a.g.off_k_norm);
+        r.norm = ld_u16(m + a.g.m_norm);
     }
-    load_codes<VBITS>(s + a.g.off_v_data, lane, r.vc);
-    r.scale = ld_u16(s + a.g.off_v_scale);
-    r.zero = ld_u16(s + a.g.off_v_zero);
+    load_codes<VBITS>(s + a.g.v_off, lane, r.vc);
+    r.scale = ld_u16(m + a.g.m_scale);
+    r.zero = ld_u16(m + a.g.m_zero);
 }
 
 // Lane l of the warp writes dims 4l .. 4l+3 of one kv head's K and V rows.
@@ -184,18 +187,21 @@ __global__ void __launch_bounds__(32 * kDqWarps) dequant_kernel(DqArgs a)
             }
             continue;
         }
-        const uint8_t* row = a.cache + slot * Hk * S;
+        // the token's records: data at dbase + h * ds, metadata at mbase + h * ms
+        const uint8_t *dbase, *mbase;
+        slot_ptrs(a.g, a.cache, slot / a.bs, int(slot % a.bs), 0, a.bs, Hk, dbase, mbase);
+        const int ds = a.g.soa ? a.g.data_bytes : S, ms = a.g.soa ? a.g.meta_bytes : S;
         int h = 0;
         for (; h + 1 < Hk; h += 2) {
             PairRaw<KBITS, VBITS> r0, r1;
-            load_pair(a, row + h * S, lane, r0);
-            load_pair(a, row + (h + 1) * S, lane, r1);
+            load_pair(a, dbase + h * ds, mbase + h * ms, lane, r0);
+            load_pair(a, dbase + (h + 1) * ds, mbase + (h + 1) * ms, lane, r1);
             finish_pair<TO>(a, kr + h * kHeadDim, vr + h * kHeadDim, lane, cl, sg4, r0);
             finish_pair<TO>(a, kr + (h + 1) * kHeadDim, vr + (h + 1) * kHeadDim, lane, cl, sg4, r1);
         }
         if (h < Hk) {
             PairRaw<KBITS, VBITS> r0;
-            load_pair(a, row + h * S, lane, r0);
+            load_pair(a, dbase + h * ds, mbase + h * ms, lane, r0);
             finish_pair<TO>(a, kr + h * kHeadDim, vr + h * kHeadDim, lane, cl, sg4, r0);
         }
     }
@@ -276,7 +282,8 @@ extern "C" int tq_dequant(int preset, int head_dim, int num_tokens, int num_kv_h
     a.vout = value_out;
     a.k_stride = key_stride_tok;
     a.v_stride = value_stride_tok;
-    a.g = geom_of(L);
+    a.bs = block_size;
+    a.g = geom_of(L, is_soa(preset));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e = out_dtype == TQ_F32 ? launch_dq<float>(a, num_tokens, st)
                           : out_dtype == TQ_F16 ? launch_dq<__half>(a, num_tokens, st)

@@ -13,6 +13,8 @@ namespace tq {
 int fill_layout(int preset, int head_dim, tq_layout* L)
 {
     if (!L || head_dim <= 0 || head_dim % 8) return TQ_ERR_INVALID_ARG;
+    if (!layout_flags_ok(preset)) return TQ_ERR_UNSUPPORTED;
+    preset &= 0xFF;                    // the block convention does not change the slot
     std::memset(L, 0, sizeof(*L));
     // Preset table: "turboquant_attn.py" supported_kv_cache_dtypes; key/value
     // widths as the preset names spell them (k8 = FP8 keys, v4 = 4-bit values,
@@ -122,7 +124,7 @@ extern "C" int tq_decode_pick_splits(int preset, int head_dim, int batch, int nu
     const int rc = tq::fill_layout(preset, head_dim, &L);
     if (rc) return rc;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return TQ_ERR_INVALID_ARG;
-    return tq::pick_splits(L, batch, num_q_heads, num_kv_heads, max_seq_len);
+    return tq::pick_splits(L, tq::is_soa(preset), batch, num_q_heads, num_kv_heads, max_seq_len);
 }
 
 extern "C" const char* tq_status_string(int status)

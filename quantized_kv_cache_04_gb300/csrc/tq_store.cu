@@ -32,6 +32,7 @@ struct StoreArgs {
     const float* midpoints;
     int num_tokens, num_kv_heads;
     int slot_size;                        // unpadded
+    int bs;                               // block_size (SoA record positions)
     SlotGeom g;
 };
 
@@ -167,9 +168,30 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
         }
         __syncthreads();
 
-        // ---------------- write the token's Hk contiguous slots
+        // ---------------- write the token's Hk contiguous slots (AoS), or its
+        // Hk data records and Hk metadata records (SoA), from the staged slots
         uint8_t* out = a.cache + slot_idx * (long long)row_bytes;
-        if ((row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+        if (a.g.soa) {
+            const int Hk = a.num_kv_heads, kd = a.g.key_data_bytes;
+            const long long page = slot_idx / a.bs;
+            const int off = int(slot_idx - page * a.bs);
+            uint8_t* blk = a.cache + page * a.bs * (long long)row_bytes;
+            uint16_t* dd = reinterpret_cast<uint16_t*>(blk + (long long)off * Hk * a.g.data_bytes);
+            uint16_t* md = reinterpret_cast<uint16_t*>(blk + (long long)a.bs * Hk * a.g.data_bytes +
+                                                       (long long)off * Hk * a.g.meta_bytes);
+            const int dh = a.g.data_bytes / 2, mh = a.g.meta_bytes / 2;
+            for (int i = threadIdx.x; i < Hk * dh; i += blockDim.x) {
+                const int hh = i / dh, j = 2 * (i - hh * dh);
+                const int src = hh * S + (j < kd ? j : a.g.off_v_data + (j - kd));
+                dd[i] = *reinterpret_cast<const uint16_t*>(row + src);
+            }
+            for (int i = threadIdx.x; i < Hk * mh; i += blockDim.x) {
+                const int hh = i / mh, f = i - hh * mh;
+                const int fo = a.g.key_fp8 ? (f == 0 ? a.g.off_v_scale : a.g.off_v_zero)
+                                           : (f == 0 ? a.g.off_k_norm : f == 1 ? a.g.off_v_scale : a.g.off_v_zero);
+                md[i] = *reinterpret_cast<const uint16_t*>(row + hh * S + fo);
+            }
+        } else if ((row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
             const uint4* src4 = reinterpret_cast<const uint4*>(row);
             uint4* dst4 = reinterpret_cast<uint4*>(out);
             for (int i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) dst4[i] = src4[i];
@@ -188,7 +210,7 @@ cudaError_t launch_store_t(int preset, const StoreArgs& a, cudaStream_t st)
     const int threads = 32 * a.num_kv_heads;
     const size_t smem = size_t(a.num_kv_heads) * a.g.slot;
     int grid = a.num_tokens < kNumSMs * 8 ? a.num_tokens : kNumSMs * 8;
-    switch (preset) {
+    switch (preset & 0xFF) {
     case TQ_K8V4:    store_kernel<T, true, 4, 4, false><<<grid, threads, smem, st>>>(a); break;
     case TQ_4BIT_NC: store_kernel<T, false, 4, 4, true><<<grid, threads, smem, st>>>(a); break;
     case TQ_K3V4_NC: store_kernel<T, false, 3, 4, true><<<grid, threads, smem, st>>>(a); break;
@@ -239,7 +261,8 @@ extern "C" int tq_store(int preset, int head_dim, int num_tokens, int num_kv_hea
     a.num_tokens = num_tokens;
     a.num_kv_heads = num_kv_heads;
     a.slot_size = L.slot_size;
-    a.g = geom_of(L);
+    a.bs = block_size;
+    a.g = geom_of(L, is_soa(preset));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = in_dtype == TQ_F16 ? launch_store_t<__half>(preset, a, st)
                                        : launch_store_t<__nv_bfloat16>(preset, a, st);

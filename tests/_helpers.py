@@ -120,3 +120,24 @@ def paged_problem(orc, preset, seq_lens, Hk, bs, rng, dtype="float16", kscale=1.
             sm = bt[b, t // bs].astype(np.int64) * bs + t % bs
             orc.store(preset, to_f32(k), to_f32(v), sm, cache, bs, s, c32, m32)
     return dict(cache=cache, bt=bt, K=Ks, V=Vs, signs=s, c32=c32, m32=m32, guard=guard)
+
+
+def aos_to_soa(orc, preset, cache):
+    """Re-arrange an AoS cache (num_blocks, bs, Hk, slot) into the SoA byte
+    convention, written out from its definition: per block, a data region of
+    [key data][value data] records, record (t, h) at index t*Hk + h, then a
+    metadata region of uint16 [k_norm][v_scale][v_zero] records
+    ([v_scale][v_zero] for FP8 keys) in the same order."""
+    L = orc.layout(preset & 0xFF)
+    nb, bs, Hk, S = cache.shape
+    kd, vd = L["key_data_bytes"], L["value_data_bytes"]
+    fields = ([L["off_v_scale"], L["off_v_zero"]] if L["key_fp8"]
+              else [L["off_k_norm"], L["off_v_scale"], L["off_v_zero"]])
+    out = np.zeros_like(cache).reshape(nb, -1)
+    rec = cache.reshape(nb, bs * Hk, S)
+    data = np.concatenate([rec[:, :, :kd], rec[:, :, L["off_v_data"]:L["off_v_data"] + vd]], axis=2)
+    meta = np.concatenate([rec[:, :, f:f + 2] for f in fields], axis=2)
+    db, mb = kd + vd, 2 * len(fields)
+    out[:, :bs * Hk * db] = data.reshape(nb, -1)
+    out[:, bs * Hk * db:bs * Hk * (db + mb)] = meta.reshape(nb, -1)
+    return out.reshape(cache.shape)

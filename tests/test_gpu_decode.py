@@ -226,3 +226,22 @@ def test_sparse_v_within_bound(orc, preset, G, Hk, bs):
         if mass.max() > 1e-6:
             assert not np.array_equal(o, o0), f"tau {tau}: nothing dropped"
 
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+@pytest.mark.parametrize("G,Hk,bs,seq_lens", [(4, 8, 16, [300, 77]), (8, 8, 64, [500, 1]),
+                                               (4, 2, 32, [129, 40]), (2, 16, 16, [90])])
+def test_decode_soa_cache(orc, preset, G, Hk, bs, seq_lens):
+    """Decode over a cache in the SoA block convention (the oracle's cache
+    re-arranged per the SoA definition) matches the oracle's attention."""
+    from _helpers import aos_to_soa
+    rng = np.random.default_rng(6300 + 10 * preset + Hk)
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng)
+    B = len(seq_lens)
+    q = torch.from_numpy(rng.normal(size=(B, G * Hk, 128)) * 1.5).to(torch.float16)
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], pb["bt"],
+                                    np.asarray(seq_lens, np.int32), Hk, bs, pb["signs"], pb["c32"])
+    soa = aos_to_soa(orc, preset, pb["cache"])
+    out, lse = _gpu_decode(preset | tq.TQ_LAYOUT_SOA, q, soa, pb["bt"], seq_lens, Hk, bs,
+                           pb["signs"], pb["c32"])
+    check_decode(out, lse, ref_o, ref_l, f"soa preset {preset} G {G} Hk {Hk}")

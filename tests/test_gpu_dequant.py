@@ -161,3 +161,21 @@ def test_dequant_full_size_sampled(orc):
                     torch.float16, rows=range(len(rows)))
         del c, ko, vo
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("preset", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("Hk,bs", [(8, 16), (3, 64)])
+def test_dequant_soa_cache(orc, preset, Hk, bs):
+    """Dequantisation of a cache in the SoA block convention equals the
+    oracle's dequantisation of the same slots in AoS form."""
+    from _helpers import aos_to_soa
+    rng = np.random.default_rng(7500 + 10 * preset + Hk)
+    seq_lens = [60, 33]
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng)
+    slots = np.concatenate([pb["bt"][b, np.arange(n) // bs].astype(np.int64) * bs + np.arange(n) % bs
+                            for b, n in enumerate(seq_lens)] + [np.array([-1], np.int64)])
+    soa = aos_to_soa(orc, preset, pb["cache"])
+    k, v = _gpu_dequant(preset | tq.TQ_LAYOUT_SOA, soa, slots, Hk, bs, pb["signs"], pb["c32"],
+                        torch.float32)
+    _check_rows(orc, preset, pb["cache"], slots, Hk, bs, pb["signs"], pb["c32"], k, v,
+                torch.float32)

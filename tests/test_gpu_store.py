@@ -122,3 +122,24 @@ def test_store_padding_only_and_large_batch(orc):
     flips, codes = compare_store(orc, preset, rows, to_f32(K[pick]).reshape(-1, 128),
                                  to_f32(V[pick]).reshape(-1, 128), s, c32, m32)
     assert flips <= max(1, math.ceil(TIE_FRACTION * codes))
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+@pytest.mark.parametrize("Hk,bs", [(8, 16), (3, 32), (1, 64)])
+def test_store_soa_is_the_aos_rearranged(orc, preset, Hk, bs):
+    """The SoA store (TQ_LAYOUT_SOA) writes, from the same inputs, exactly the
+    bytes of the AoS store re-arranged per the SoA definition (blocks never
+    written keep their contents in both)."""
+    from _helpers import aos_to_soa
+    rng = np.random.default_rng(6200 + 10 * preset + Hk)
+    N, nb = 150, 12
+    K = torch.from_numpy(rng.normal(size=(N, Hk, 128))).to(torch.float16)
+    V = torch.from_numpy(rng.normal(size=(N, Hk, 128))).to(torch.float16)
+    sm = rng.permutation(nb * bs)[:N].astype(np.int64)
+    sm[::17] = -1
+    aos, *_ = _run_store(orc, preset, K, V, sm, nb, bs)
+    soa, *_ = _run_store(orc, preset | tq.TQ_LAYOUT_SOA, K, V, sm, nb, bs)
+    touched = np.unique(sm[sm >= 0] // bs)
+    assert np.array_equal(soa[touched], aos_to_soa(orc, preset, aos[touched]))
+    rest = np.setdiff1d(np.arange(nb), touched)
+    assert np.all(soa[rest] == SENTINEL)

@@ -148,3 +148,30 @@ def test_store_paging_and_padding(orc):
             assert np.array_equal(flat[sm[t], h], ref)
     untouched = np.setdiff1d(np.arange(nb * bs), sm[sm >= 0])
     assert np.all(flat[untouched] == 0xAB)
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_soa_store_is_a_rearrangement(orc, preset):
+    """The oracle's SoA store writes the same slot bytes as its AoS store, in
+    the places the SoA definition gives (an independent numpy re-arrangement),
+    and its decode reads them back to the same attention."""
+    from _helpers import aos_to_soa
+    rng = np.random.default_rng(5150 + preset)
+    D, Hk, bs, N = 128, 3, 16, 40
+    L = orc.layout(preset)
+    s = orc.signs(D, 42)
+    c32, m32 = (np.zeros(1, np.float32),) * 2 if L["key_fp8"] else orc.codebook(D, L["key_bits"])
+    k = rng.normal(size=(N, Hk, D)).astype(np.float32)
+    v = rng.normal(size=(N, Hk, D)).astype(np.float32)
+    sm = rng.permutation(3 * bs)[:N].astype(np.int64)
+    aos = np.zeros((3, bs, Hk, L["slot_size_aligned"]), np.uint8)
+    soa = np.zeros_like(aos)
+    orc.store(preset, k, v, sm, aos, bs, s, c32, m32)
+    orc.store(preset | orc.LAYOUT_SOA, k, v, sm, soa, bs, s, c32, m32)
+    assert np.array_equal(soa, aos_to_soa(orc, preset, aos))
+    q = rng.normal(size=(1, 2 * Hk, D)).astype(np.float32)
+    bt = np.array([[0, 1, 2]], np.int32)
+    sl = np.array([3 * bs], np.int32)
+    o1, l1 = orc.decode_dense(preset, q, aos, bt, sl, Hk, bs, s, c32)
+    o2, l2 = orc.decode_dense(preset | orc.LAYOUT_SOA, q, soa, bt, sl, Hk, bs, s, c32)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
