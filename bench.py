@@ -53,6 +53,8 @@ def _args():
     p.add_argument("--ctx", type=int, default=None)
     p.add_argument("--batch", type=int, default=None)
     p.add_argument("--splits", type=int, default=None, help="0 = library picks")
+    p.add_argument("--soa", action="store_true",
+                   help="cache blocks in the SoA byte convention (TQ_LAYOUT_SOA)")
     p.add_argument("--v-threshold", type=float, default=0.0,
                    help="sparse V: rows with softmax factor <= this skip the value sum (0 = dense)")
     p.add_argument("--e2e-steps", type=int, default=None)
@@ -164,12 +166,13 @@ def _traffic(workload: str, kernel: str):
 class Problem:
     """Device-resident cache, queries and per-step inputs of one workload."""
 
-    def __init__(self, w, dev, splits, v_threshold: float = 0.0):
+    def __init__(self, w, dev, splits, v_threshold: float = 0.0, soa: bool = False):
         import torch
         import quantized_kv_cache_04_gb300 as tq
         self.w, self.dev = w, dev
         self.vthr = float(v_threshold)
-        self.c = tq.TQCache(w.preset, w.num_blocks, w.block_size, w.Hk, device=dev)
+        self.c = tq.TQCache(w.preset_id | (tq.TQ_LAYOUT_SOA if soa else 0), w.num_blocks,
+                            w.block_size, w.Hk, device=dev)
         self.c.cache[w.guard_block] = 0xFF          # never read if paging is right
         CH = 32768
         for b in range(w.B):
@@ -496,7 +499,7 @@ def main():
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
 
-    p = Problem(w, dev, args.splits, args.v_threshold)
+    p = Problem(w, dev, args.splits, args.v_threshold, args.soa)
     assert args.warmup >= 3
     total_ms, dec_ms, clocks = time_device(p, args.steps, args.warmup, world, gpu_index)
     step_ms = _max_over_ranks(total_ms / args.steps, world)
@@ -518,7 +521,8 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": _describe(w), "preset": w.preset, "batch": w.B,
                    "seq_len": int(w.seq_lens.max()), "block_size": w.block_size,
-                   "num_splits": p.S, "sparse_v_threshold": args.v_threshold, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "num_splits": p.S, "sparse_v_threshold": args.v_threshold,
+                   "block_layout": "soa" if args.soa else "aos", "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": f"inputs larger than L2 ({kvb / 1e6:.0f} MB packed KV > 129 MiB L2)"
                    if kvb > L2_BYTES else "inputs smaller than L2 (not flushed)"},
         "e2e": {"value": round(world * kvb / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",

@@ -1,0 +1,872 @@
+// Decode stage 1 on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate).
+//
+// Same partials as the CUDA-core stage 1 (per split: o_s and lse_s in the
+// fp32 workspace), computed per CTA = (split, sequence) over all kv heads:
+// one warp per kv head, 32-token tiles streamed into a shared-memory ring by
+// bulk (TMA) copies of whole token rows (Hk contiguous slots each) whose
+// completion is tracked by mbarriers with bounded waits; warps only wait for
+// data, never for each other (the last warp done with a stage refills it).
+//
+// Per tile and warp, with G query heads sharing the kv head:
+//   scores  S[t, g] = sum_d K^[t, d] Q[g, d]      A = K^ (16 tokens x 16 dims),
+//                                                B = q columns (16 dims x 8)
+//   values  O[d, g] += sum_t V^[t, d] P'[t, g]    A = V codes (16 dims x 16 tokens),
+//                                                B = P' columns (16 tokens x 8)
+// The grouped-query tiles are dense after unpacking, so they run as MMAs.
+// Precision: fp16 operands carry 11 bits, so every fp32 quantity that is not
+// exactly representable is split into hi = fp16(x) and lo = fp16(x - hi):
+// q (all presets), the Lloyd-Max centroids of MSE keys, and P' (for G = 4 the
+// spare 4 columns carry the lo parts; for G = 8 a second MMA does).  FP8 keys and integer value codes
+// are exact in fp16.  The value path uses P' = p * v_scale and adds
+// sum_t p_t v_zero_t separately (v_hat = code * scale + zero).
+//
+// Method sources: "vllm-project/vllm pull 38479" digest, implementation item 4
+// (split-K stage 1 / stage 2); "vllm.v1.attention.backends.turboquant_attn" API
+// page, "_decode_attention" (GQA grouping, fixed split count);
+// "turboquant-plus.md", weight pre-rotation note (<Q H, H K> = <Q, K>).
+#include "tq.h"
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+#include <cmath>
+#include <type_traits>
+
+namespace tq {
+
+struct MmaArgs {
+    const void* query;
+    const uint8_t* cache;
+    const int32_t* block_table;
+    int bt_stride;
+    const int32_t* seq_lens;
+    float qscale;            // softmax_scale * log2(e): scores in log2 units
+    int num_splits;
+    const int8_t* signs;
+    const float* centroids;
+    float* mid;              // (B, Hq, S, D+1)
+    int Hq, Hk, G, bs, bs_log2;
+    int row_bytes;           // global token row: Hk * slot
+    int hpc;                 // kv heads per CTA (Hk, or 4 for FP8 keys)
+    int copy_bytes;          // AoS: hpc * slot; SoA: hpc * data record (the data part a CTA copies)
+    int smem_row;            // copy_bytes padded to 16 mod 32 bytes
+    int meta_bytes;          // SoA: hpc * metadata record per token (0 for AoS)
+    int nstages;
+    float vthr;              // sparse V: rows with p <= vthr skip the value sum (0: off)
+    SlotGeom g;
+};
+
+// Stage 1 with the value sum of every row (dense) or with the sparse-V gate;
+// each is instantiated in its own translation unit.
+cudaError_t launch_mma_dense(const MmaArgs& a, int q_dtype, int B, size_t smem, cudaStream_t st);
+cudaError_t launch_mma_sparse(const MmaArgs& a, int q_dtype, int B, size_t smem, cudaStream_t st);
+
+namespace {
+
+constexpr int kTile = 32;   // tokens per pipeline stage (two 16-row MMA tiles)
+constexpr uint32_t kWaitLimit = 1u << 24;   // mbarrier polls before a stage wait gives up
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// hi/lo fp16 split of x: x ~= hi + lo with |x - hi - lo| ~ 2^-22 |x|
+__device__ __forceinline__ void split_f16(float x, float& hi, float& lo)
+{
+    hi = __half2float(__float2half_rn(x));
+    lo = x - hi;
+}
+
+// ---- bulk (TMA) copies into shared memory, completion tracked by mbarriers
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity, giving up after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit)
+{
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// n little-endian 32-bit words starting at the 2-byte aligned shared address p.
+// `mis` (0 or 2, uniform per warp) is p mod 4; ALIGNED promises mis == 0.
+template <int N, bool ALIGNED = false>
+__device__ __forceinline__ void lds_words(const uint8_t* p, int mis, uint32_t (&w)[N])
+{
+    if (ALIGNED || mis == 0) {
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = q[i];
+    } else {
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(p - mis);
+        uint32_t r[N + 1];
+#pragma unroll
+        for (int i = 0; i <= N; ++i) r[i] = q[i];
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], 16);
+    }
+}
+
+__device__ __forceinline__ float lds_f16(const uint8_t* p)
+{
+    return __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(p)));
+}
+
+// 3-bit group (32 codes in words W0..W2): nibble words of codes 0-7, 8-15,
+// 16-23, 24-31 with every nibble's top bit clear.
+__device__ __forceinline__ void nibbles3(const uint32_t (&w)[3], uint32_t (&n)[4])
+{
+    n[0] = w[0] & 0x77777777u;
+    n[1] = w[1] & 0x77777777u;
+    n[2] = w[2] & 0x77777777u;
+    n[3] = ((w[0] >> 3) & 0x11111111u) | ((w[1] >> 2) & 0x22222222u) | ((w[2] >> 1) & 0x44444444u);
+}
+
+// Token of QK row r (0..15) inside a tile.  Rows r and r+8 of a thread hold
+// tokens whose shared-memory rows are 8 apart modulo 8 (fewer bank
+// conflicts), and the four tokens 4m..4m+3 that one PV thread needs come
+// from exactly two QK threads.
+__device__ __forceinline__ int qk_token(int r)
+{
+    const int gid = r & 7, m = gid >> 1, e = gid & 1;
+    const bool second = r >= 8;
+    const bool hi_pair = (m >= 2) != second;   // +2 for (m<2, second row) or (m>=2, first row)
+    return 4 * m + e + (hi_pair ? 2 : 0);
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two_bytes)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu),
+                                                     __NV_E4M3);
+    return uint32_t(h.x) | (uint32_t(h.y) << 16);
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// two E4M3 pairs (low and high half of w) -> two f16x2
+__device__ __forceinline__ void cvt_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// 16-entry centroid lookup (4-bit keys) of the four codes in the low 16 bits
+// of s (code j in nibble j).  PRMT indexes 8 bytes, so each byte plane has a
+// table for codes 0-7 (T[2p]) and one for codes 8-15 (T[2p + 1]); both are
+// read with the low 3 bits of every code and a third PRMT keeps, per byte,
+// the one that bit 3 names.  Planes: 0/1 = low/high byte of fp16(c), 2/3 =
+// low/high byte of the fp16 residual.  h0/h1 (l0/l1): the hi (lo) halves of
+// codes 0,1 and 2,3 as half2.
+__device__ __forceinline__ void lut16(const uint32_t (&T)[8][2], uint32_t s, uint32_t& h0, uint32_t& h1,
+                                      uint32_t& l0, uint32_t& l1)
+{
+    const uint32_t s7 = s & 0x7777u;
+    const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;   // byte j from the second word if bit 3 set
+    uint32_t x[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        x[p] = prmt(prmt(T[2 * p][0], T[2 * p][1], s7), prmt(T[2 * p + 1][0], T[2 * p + 1][1], s7), pick);
+    h0 = prmt(x[0], x[1], 0x5140u);
+    h1 = prmt(x[0], x[1], 0x7362u);
+    l0 = prmt(x[2], x[3], 0x5140u);
+    l1 = prmt(x[2], x[3], 0x7362u);
+}
+
+// Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1: row gid+8).
+// Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
+template <int KMODE, int G, int NT>
+__device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
+                                        const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
+                                        const uint32_t (&T)[NT][2], float (&out)[4], float (&outl)[4])
+{
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float scl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (KMODE == 8) {
+        const uint32_t* k0p = reinterpret_cast<const uint32_t*>(r0 + 4 * tig);
+        const uint32_t* k1p = reinterpret_cast<const uint32_t*>(r1 + 4 * tig);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t A[4];
+            cvt_e4m3x4(k0p[4 * kk], A[0], A[2]);
+            cvt_e4m3x4(k1p[4 * kk], A[1], A[3]);
+            mma16816(sc[kk & 1], A, bq[kk][0], bq[kk][1]);
+            if constexpr (G == 8) mma16816(scl[kk & 1], A, bql[kk][0], bql[kk][1]);
+        }
+    } else {
+        // one 32-code group (3-bit: 12 bytes, 4-bit: 16 bytes) of each row per
+        // thread, as four nibble words of 8 codes (k-step kk uses 4 of them)
+        uint32_t c0[4], c1[4];
+        if constexpr (KMODE == 3) {
+            uint32_t w0[3], w1[3];
+            lds_words<3>(r0 + 12 * tig, kmis, w0);
+            lds_words<3>(r1 + 12 * tig, kmis, w1);
+            nibbles3(w0, c0);
+            nibbles3(w1, c1);
+        } else if constexpr (KMODE == 2) {
+            // 32 two-bit codes = two words; the even codes of a word go to one
+            // nibble word and the odd codes to another (code 2i / 2i + 1 of
+            // the word in nibble i), so k-step kk covers dims with stride 2
+            uint32_t w0[2], w1[2];
+            lds_words<2>(r0 + 8 * tig, kmis, w0);
+            lds_words<2>(r1 + 8 * tig, kmis, w1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                c0[2 * i] = w0[i] & 0x33333333u;
+                c0[2 * i + 1] = (w0[i] >> 2) & 0x33333333u;
+                c1[2 * i] = w1[i] & 0x33333333u;
+                c1[2 * i + 1] = (w1[i] >> 2) & 0x33333333u;
+            }
+        } else {
+            lds_words<4>(r0 + 16 * tig, kmis, c0);
+            lds_words<4>(r1 + 16 * tig, kmis, c1);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t s0 = c0[kk >> 1] >> (16 * (kk & 1));
+            const uint32_t s1 = c1[kk >> 1] >> (16 * (kk & 1));
+            uint32_t Ahi[4], Alo[4];
+            if constexpr (KMODE == 4) {
+                lut16(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
+                lut16(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
+            } else {
+                // 2- and 3-bit keys: one lookup per byte plane, then interleave
+                // the low and high bytes into half2 registers
+                const uint32_t p0 = prmt(T[0][0], T[0][1], s0), p1 = prmt(T[1][0], T[1][1], s0);
+                const uint32_t q0 = prmt(T[0][0], T[0][1], s1), q1 = prmt(T[1][0], T[1][1], s1);
+                Ahi[0] = prmt(p0, p1, 0x5140u);
+                Ahi[2] = prmt(p0, p1, 0x7362u);
+                Ahi[1] = prmt(q0, q1, 0x5140u);
+                Ahi[3] = prmt(q0, q1, 0x7362u);
+                const uint32_t u0 = prmt(T[2][0], T[2][1], s0), u1 = prmt(T[3][0], T[3][1], s0);
+                const uint32_t v0 = prmt(T[2][0], T[2][1], s1), v1 = prmt(T[3][0], T[3][1], s1);
+                Alo[0] = prmt(u0, u1, 0x5140u);
+                Alo[2] = prmt(u0, u1, 0x7362u);
+                Alo[1] = prmt(v0, v1, 0x5140u);
+                Alo[3] = prmt(v0, v1, 0x7362u);
+            }
+            if constexpr (G == 4) {
+                mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
+                mma16816(sc[1], Alo, bq[kk][0], bq[kk][1]);
+            } else {
+                mma16816(sc[kk & 1], Ahi, bq[kk][0], bq[kk][1]);
+                mma16816(scl[0], Ahi, bql[kk][0], bql[kk][1]);
+                mma16816(scl[1], Alo, bq[kk][0], bq[kk][1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[i] = sc[0][i] + sc[1][i];
+        outl[i] = scl[0][i] + scl[1][i];
+    }
+}
+
+// P' of one 16-row tile to the B layout of the value MMA: thread (gid, tig)
+// feeds column gid for tokens 4 tig .. 4 tig + 3, which QK threads with
+// gid 2 tig and 2 tig + 1 hold (first row = qk_token(gid), second = qk_token(gid + 8)).
+// pp[j][r]: P' of the thread's head j (G = 8: heads 2 tig, 2 tig + 1), row r.
+template <int G>
+__device__ __forceinline__ void p_to_b(const float (&pp)[G == 8 ? 2 : 1][2], int gid, int tig,
+                                       uint32_t (&pb)[2][2])
+{
+    uint32_t Xh, Yh, Xl, Yl;
+    if constexpr (G == 4) {
+        float h0, l0, h1, l1;
+        split_f16(pp[0][0], h0, l0);
+        split_f16(pp[0][1], h1, l1);
+        Xh = pack_half2(h0, h1);        // column (head, hi)
+        Yh = pack_half2(l0, l1);        // column (head, lo)
+        Xl = Yl = 0u;
+    } else {
+        float h0, l0, h1, l1, h2, l2, h3, l3;
+        split_f16(pp[0][0], h0, l0);
+        split_f16(pp[0][1], h1, l1);
+        split_f16(pp[1][0], h2, l2);
+        split_f16(pp[1][1], h3, l3);
+        Xh = pack_half2(h0, h1);
+        Yh = pack_half2(h2, h3);
+        Xl = pack_half2(l0, l1);
+        Yl = pack_half2(l2, l3);
+    }
+    const int src_tig = gid >> 1;
+    const bool take_y = gid & 1;
+    const int srcA = 4 * (2 * tig) + src_tig, srcB = 4 * (2 * tig + 1) + src_tig;
+    constexpr int NP = G == 4 ? 1 : 2;
+#pragma unroll
+    for (int part = 0; part < NP; ++part) {
+        const uint32_t X = part ? Xl : Xh, Y = part ? Yl : Yh;
+        const uint32_t ax = __shfl_sync(0xffffffffu, X, srcA), ay = __shfl_sync(0xffffffffu, Y, srcA);
+        const uint32_t bx = __shfl_sync(0xffffffffu, X, srcB), by = __shfl_sync(0xffffffffu, Y, srcB);
+        const uint32_t XA = take_y ? ay : ax, XB = take_y ? by : bx;
+        if (tig < 2) { pb[part][0] = prmt(XA, XB, 0x5410u); pb[part][1] = prmt(XA, XB, 0x7632u); }
+        else         { pb[part][0] = prmt(XA, XB, 0x7632u); pb[part][1] = prmt(XA, XB, 0x5410u); }
+    }
+}
+
+// Value MMAs of one 16-row tile: tokens 4 tig + j of the tile, dims 16 gid + 2i (+1).
+// A value code n (0..15) placed alone in a byte and read as FP8 E4M3 is
+// exactly n * 2^-9 (subnormal for n < 8, normal above), and that is a normal
+// fp16 number: one conversion instruction turns two such bytes into the
+// half2 of an A register.  The accumulators therefore hold 2^-9 of the value
+// sums; the epilogue scales them back by 512 (exact).
+template <int VBITS, int G, bool ALIGNED>
+__device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, int tig, int vmis,
+                                        const uint32_t (&pb)[2][2], float (&acc)[8][4])
+{
+    uint32_t vw[4][2];   // per token 4 tig + j: nibble words of dims 16 gid .. 16 gid + 15
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint8_t* rv = tile_v + (4 * tig + j) * rs;
+        if constexpr (VBITS == 4) {
+            lds_words<2, ALIGNED>(rv + 8 * gid, vmis, vw[j]);
+        } else if constexpr (VBITS == 2) {
+            uint32_t w[1];
+            lds_words<1, ALIGNED>(rv + 4 * gid, vmis, w);
+            vw[j][0] = w[0];
+            vw[j][1] = 0u;
+        } else {
+            uint32_t w[3], n[4];
+            lds_words<3, ALIGNED>(rv + 12 * (gid >> 1), vmis, w);
+            nibbles3(w, n);
+            vw[j][0] = (gid & 1) ? n[2] : n[0];
+            vw[j][1] = (gid & 1) ? n[3] : n[1];
+        }
+    }
+    // MMAs i and i + 1 (dims 16 gid + 2i .. 2i + 3) share one byte gather:
+    // ab = [A_i, B_i, A_i+1, B_i+1] with A, B the tokens of k = 2 tig, 2 tig + 1
+    // (cd likewise for tokens 4 tig + 2, + 3); its low nibbles give row gid
+    // (even dims), its high nibbles row gid + 8 (odd dims).
+    if constexpr (VBITS == 2) {
+        // byte b of a token's word holds dims 16 gid + 4b .. 4b + 3 (two bits
+        // each): ab = [A_b, B_b, A_b+1, B_b+1] feeds MMAs 2b .. 2b + 3
+#pragma unroll
+        for (int i = 0; i < 8; i += 4) {
+            const uint32_t c = uint32_t(i >> 1);
+            const uint32_t sel = c | ((c + 4) << 4) | ((c + 1) << 8) | ((c + 5) << 12);
+            const uint32_t ab = prmt(vw[0][0], vw[1][0], sel);
+            const uint32_t cd = prmt(vw[2][0], vw[3][0], sel);
+            uint32_t A[4][4];            // MMAs i .. i + 3
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // two-bit field q of each byte: dim 2i + q (+4 in the high half)
+                const uint32_t m = 0x03030303u;
+                const int mma = (q >> 1), row = q & 1;
+                cvt_e4m3x4((ab >> (2 * q)) & m, A[mma][row], A[mma + 2][row]);
+                cvt_e4m3x4((cd >> (2 * q)) & m, A[mma][row + 2], A[mma + 2][row + 2]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                mma16816(acc[i + u], A[u], pb[0][0], pb[0][1]);
+                if constexpr (G == 8) mma16816(acc[i + u], A[u], pb[1][0], pb[1][1]);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const uint32_t c = uint32_t(i & 3);
+        const uint32_t sel = c | ((c + 4) << 4) | ((c + 1) << 8) | ((c + 5) << 12);
+        const uint32_t ab = prmt(vw[0][i >> 2], vw[1][i >> 2], sel);
+        const uint32_t cd = prmt(vw[2][i >> 2], vw[3][i >> 2], sel);
+        uint32_t A0[4], A1[4];
+        cvt_e4m3x4(ab & 0x0F0F0F0Fu, A0[0], A1[0]);
+        cvt_e4m3x4((ab >> 4) & 0x0F0F0F0Fu, A0[1], A1[1]);
+        cvt_e4m3x4(cd & 0x0F0F0F0Fu, A0[2], A1[2]);
+        cvt_e4m3x4((cd >> 4) & 0x0F0F0F0Fu, A0[3], A1[3]);
+        mma16816(acc[i], A0, pb[0][0], pb[0][1]);
+        if constexpr (G == 8) mma16816(acc[i], A0, pb[1][0], pb[1][1]);
+        mma16816(acc[i + 1], A1, pb[0][0], pb[0][1]);
+        if constexpr (G == 8) mma16816(acc[i + 1], A1, pb[1][0], pb[1][1]);
+    }
+}
+
+// KMODE: 8 = FP8 E4M3 keys, 2 / 3 / 4 = 2- / 3- / 4-bit Lloyd-Max keys.
+// VBITS: 2, 3 or 4.
+// G: 4 (columns = 4 heads x {hi, lo}) or 8 (columns = 8 heads).
+// One CTA = (split, sequence); warp w = kv head w; each iteration consumes a
+// 32-token tile (two 16-row MMA tiles) with one softmax update.
+template <typename TQ, int KMODE, int VBITS, int G, bool SOA, bool SPARSE>
+__global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int split = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h0 = blockIdx.z * a.hpc;        // first kv head of this CTA
+    const int h = h0 + warp;                   // this warp's kv head
+    const int S = a.num_splits, Hq = a.Hq, Greal = a.G;
+    const int Hc = a.hpc;
+    const int nwarps = blockDim.x >> 5;
+
+    const int L = a.seq_lens[b];
+    int chunk = (L + S - 1) / S;
+    chunk = (chunk + kTile - 1) / kTile * kTile;
+    const int t_begin = split * chunk;
+    const int t_end = min(L, t_begin + chunk);
+
+    if (t_begin >= t_end) {      // empty split: lse = -inf and a zero partial
+        for (int i = threadIdx.x; i < Hc * Greal * (kHeadDim + 1); i += blockDim.x) {
+            const int hq = h0 * Greal + i / (kHeadDim + 1), d = i % (kHeadDim + 1);
+            float* m = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
+            m[d] = d == kHeadDim ? -INFINITY : 0.f;
+        }
+        return;
+    }
+
+    // ---------------- shared-memory ring of 32 token rows (the CTA's kv
+    // heads), filled by bulk (TMA) copies.  Rows of one page are contiguous in
+    // global memory: one copy per page segment when the CTA takes whole rows
+    // and the shared row stride equals the global one, else one copy per row
+    // (issued by the 32 lanes of one warp).
+    const int row_bytes = a.row_bytes;        // global token row (Hk slots)
+    const int cb = a.copy_bytes;              // bytes of it this CTA copies (SoA: data part)
+    const int rs = a.smem_row;                // shared row stride: 16 mod 32 bytes
+    const int mb = SOA ? a.meta_bytes : 0;    // SoA: metadata part per token, rows after the data rows
+    const int stage_bytes = kTile * (rs + mb);
+    const int NST = a.nstages;
+    const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
+    const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
+    const int lg = a.bs_log2;
+    const int seg_rows = kTile < (1 << lg) ? kTile : (1 << lg);   // rows per page segment
+    // Per stage: `full` completes when the stage's bytes have landed; `done`
+    // counts the warps finished with it.  The warp that finishes a stage last
+    // refills it, so warps never wait on each other, only on data.
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * stage_bytes);
+    int* done = reinterpret_cast<int*>(full + NST);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); done[i] = 0; }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // Only rows of tokens < L are copied: block-table entries past the
+    // sequence's last page are never read.  Skipped rows keep stale bytes and
+    // are masked out of the softmax.
+    // SoA blocks: the token rows' data parts and metadata parts lie in two
+    // regions of the block; each row (or page segment) takes one copy per
+    // region, the metadata landing in rows of mb bytes after the data rows.
+    constexpr bool soa = SOA;                  // the block convention (a.g.soa), fixed per instantiation
+    const long long hs_g = soa ? a.g.data_bytes : a.g.slot;    // head stride in a global data row
+    const long long drow = soa ? (long long)a.Hk * a.g.data_bytes : row_bytes;
+    auto issue = [&](int tile, int stage) {   // called by all lanes of one warp
+        if (tile >= ntiles) return;
+        uint8_t* dst = smem + stage * stage_bytes;
+        uint64_t* bar = &full[stage];
+        const int tbase = t_begin + tile * kTile;
+        const bool per_segment = rs == drow && cb == drow && (!soa || mb == a.Hk * a.g.meta_bytes);
+        const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile and region
+        const int seg_len = per_segment ? seg_rows : 1;               // rows per copy
+        const int nlive = min(nseg, (L - tbase + seg_len - 1) / seg_len);
+        if (lane == 0) {
+            fence_async_shared();             // prior generic reads of this stage before the async writes
+            mbar_expect_tx(bar, uint32_t(nlive * seg_len * (cb + mb)));
+        }
+        __syncwarp();
+        if (lane < nlive) {
+            const int t = tbase + lane * seg_len;
+            const long long page = bt[t >> lg];
+            const int off = t & ((1 << lg) - 1);
+            if (soa) {
+                const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
+                bulk_g2s(dst + lane * seg_len * rs, blk + off * drow + h0 * hs_g, uint32_t(seg_len * cb), bar);
+                const uint8_t* meta = blk + (1LL << lg) * drow + ((long long)off * a.Hk + h0) * a.g.meta_bytes;
+                bulk_g2s(dst + kTile * rs + lane * seg_len * mb, meta, uint32_t(seg_len * mb), bar);
+            } else {
+                const uint8_t* src = a.cache + ((page << lg) + off) * (long long)row_bytes + h0 * hs_g;
+                bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * cb), bar);
+            }
+        }
+    };
+    // The q staging area (hpc x (4 or 8) heads x 512 B) sits at the end of the
+    // ring: the tiles whose stages lie wholly before it are requested first,
+    // so their latency overlaps the preparation of q.
+    const int q_base = NST * stage_bytes - Hc * G * kHeadDim * 4;
+    const int s_q = q_base / stage_bytes;
+    if (warp == 0)
+        for (int i = 0; i < s_q; ++i) issue(i, i);
+
+    // ---------------- q columns: B operand of the score MMA.  Each warp
+    // rotates (MSE keys) and scales its G query heads with lane l holding dims
+    // 4l..4l+3, parks them in the staging area, and every thread reads back
+    // the 32 values of its column.  The k index of k-step kk and thread tig
+    // maps to dims
+    //   FP8 keys:   16 kk + 4 tig + j   one key word per k-step, bank-conflict
+    //               free across the warp
+    //   3-bit keys: 32 tig + 4 kk + j   one 32-code group (three words) per thread
+    //   4-bit keys: the same, 16 bytes per thread
+    //   2-bit keys: 32 tig + 16 (kk >> 2) + 8 (kk & 1) + ((kk >> 1) & 1) + 2 j
+    //               (8 bytes per thread; see qk_tile)
+    uint32_t bq[8][2], bql[8][2];
+    {
+        float* sq = reinterpret_cast<float*>(smem + q_base) + warp * G * kHeadDim;
+        float sgn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sgn[i] = KMODE == 8 ? 1.f : float(a.signs[4 * lane + i]);
+        const TQ* Q = static_cast<const TQ*>(a.query);
+        for (int g = 0; g < G; ++g) {
+            float qv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (g < Greal) {        // warp-uniform
+                const TQ* qp = Q + ((long long)b * Hq + h * Greal + g) * kHeadDim + 4 * lane;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qv[i] = sgn[i] * to_f32(qp[i]);
+                if constexpr (KMODE != 8) {
+                    fwht128_warp(qv, lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) qv[i] *= 0.08838834764831845f;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qv[i] *= a.qscale;
+            }
+            reinterpret_cast<float4*>(sq + g * kHeadDim)[lane] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+        }
+        __syncwarp();
+        const int col_head = G == 4 ? (gid >> 1) : gid;
+        const bool col_lo = G == 4 && (gid & 1);
+        const float* qc = sq + col_head * kHeadDim;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            float4 x;
+            if constexpr (KMODE == 2) {
+                // dims 32 tig + 16 (kk >> 2) + 8 (kk & 1) + ((kk >> 1) & 1) + 2 j
+                const float* qd = qc + 32 * tig + 16 * (kk >> 2) + 8 * (kk & 1) + ((kk >> 1) & 1);
+                x = make_float4(qd[0], qd[2], qd[4], qd[6]);
+            } else {
+                x = reinterpret_cast<const float4*>(qc + (KMODE == 8 ? 16 * kk + 4 * tig : 32 * tig + 4 * kk))[0];
+            }
+            float hi[4], lo[4];
+            split_f16(x.x, hi[0], lo[0]);
+            split_f16(x.y, hi[1], lo[1]);
+            split_f16(x.z, hi[2], lo[2]);
+            split_f16(x.w, hi[3], lo[3]);
+            if (G == 4) {
+                bq[kk][0] = col_lo ? pack_half2(lo[0], lo[1]) : pack_half2(hi[0], hi[1]);
+                bq[kk][1] = col_lo ? pack_half2(lo[2], lo[3]) : pack_half2(hi[2], hi[3]);
+                bql[kk][0] = bql[kk][1] = 0u;
+            } else {
+                bq[kk][0] = pack_half2(hi[0], hi[1]);
+                bq[kk][1] = pack_half2(hi[2], hi[3]);
+                bql[kk][0] = pack_half2(lo[0], lo[1]);
+                bql[kk][1] = pack_half2(lo[2], lo[3]);
+            }
+        }
+        __syncthreads();            // every warp is done with the staging area
+    }
+    if (warp == 0)
+        for (int i = s_q; i < NST; ++i) issue(i, i);
+
+    // ---------------- centroid byte planes for the PRMT lookup (MSE keys):
+    // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
+    // fp16 residual c - fp16(c).  2- and 3-bit keys: T[p][k >> 2] holds entries
+    // 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
+    // plane p of codes 8(k>>3) .. 8(k>>3)+7 in the same way.
+    uint32_t T[KMODE == 4 ? 8 : 4][2] = {};
+    if constexpr (KMODE != 8) {
+        constexpr int NC = 1 << KMODE;
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            const float c = a.centroids[k];
+            const __half chi = __float2half_rn(c);
+            const __half clo = __float2half_rn(c - __half2float(chi));
+            const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
+            const int sh = 8 * (k & 3), w = (k >> 2) & 1;
+            const int t = KMODE == 4 ? (k >> 3) : 0;     // table of the plane
+            const int st = KMODE == 4 ? 2 : 1;           // tables per plane
+            T[0 * st + t][w] |= (hb & 0xFFu) << sh;
+            T[1 * st + t][w] |= (hb >> 8) << sh;
+            T[2 * st + t][w] |= (lb & 0xFFu) << sh;
+            T[3 * st + t][w] |= (lb >> 8) << sh;
+        }
+    }
+
+    constexpr int NH = G == 8 ? 2 : 1;        // query heads per thread (softmax state)
+    float m_run[NH], l_run[NH], z_run[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) { m_run[j] = -INFINITY; l_run[j] = 0.f; z_run[j] = 0.f; }
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+    const int tau0 = qk_token(gid), tau1 = qk_token(gid + 8);
+    const int hoff = warp * int(hs_g);         // this warp's slot (SoA: data record) in a shared row
+    const int kmis = hoff & 2;
+    const int vmis = (hoff + a.g.v_off) & 2;
+    // metadata rows: AoS = the data rows (fields inside the slot); SoA = the
+    // rows after the data rows, mb bytes each
+    const int mrs = soa ? mb : rs;
+    const int moff = soa ? kTile * rs + warp * a.g.meta_bytes : hoff;
+
+    // One 32-token tile in stage memory st (this warp's slot at offset 0).
+    // PARTIAL: some of its tokens lie at or past t_end and are masked.
+    auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag) {
+        constexpr bool PARTIAL = decltype(partial_tag)::value;
+        // ---- scores of both 16-row tiles
+        float s[NH][2][2], vs[2][2], vz[2][2];
+        bool ok[2][2];
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+            const uint8_t* r0 = st + (16 * rt + tau0) * rs;
+            const uint8_t* r1 = st + (16 * rt + tau1) * rs;
+            const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
+            const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
+            float sc[4], scl[4];
+            qk_tile<KMODE, G>(r0, r1, tig, kmis, bq, bql, T, sc, scl);
+            float n0 = 1.f, n1 = 1.f;
+            if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
+            vs[rt][0] = lds_f16(m0 + a.g.m_scale);
+            vz[rt][0] = lds_f16(m0 + a.g.m_zero);
+            vs[rt][1] = lds_f16(m1 + a.g.m_scale);
+            vz[rt][1] = lds_f16(m1 + a.g.m_zero);
+            ok[rt][0] = !PARTIAL || t0 + 16 * rt + tau0 < t_end;
+            ok[rt][1] = !PARTIAL || t0 + 16 * rt + tau1 < t_end;
+            if constexpr (G == 4) {
+                s[0][rt][0] = (sc[0] + sc[1]) * n0;
+                s[0][rt][1] = (sc[2] + sc[3]) * n1;
+            } else {
+                s[0][rt][0] = (sc[0] + scl[0]) * n0;
+                s[1][rt][0] = (sc[1] + scl[1]) * n0;
+                s[0][rt][1] = (sc[2] + scl[2]) * n1;
+                s[1][rt][1] = (sc[3] + scl[3]) * n1;
+            }
+        }
+
+        // ---- one online-softmax update for the 32 tokens (log2 units).  The
+        // running max only moves when a head's tile max exceeds it by more
+        // than 8 (so p <= 2^8 otherwise), or when a value scale above 128
+        // could take p * v_scale out of the fp16 range of P'.  Moving it
+        // rescales the accumulators; keeping it changes no result, since
+        // o and l share the same reference.
+        float mt[NH];
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (!ok[rt][r]) s[j][rt][r] = -INFINITY;
+                    m = fmaxf(m, s[j][rt][r]);
+                }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            mt[j] = m;               // finite: the tile's first token is valid
+            need |= m > m_run[j] + 8.f;
+        }
+        need |= fmaxf(fmaxf(vs[0][0], vs[0][1]), fmaxf(vs[1][0], vs[1][1])) > 128.f;
+        if (__any_sync(0xffffffffu, need)) {
+            float alpha[NH];
+#pragma unroll
+            for (int j = 0; j < NH; ++j) {
+                const float mn = fmaxf(m_run[j], mt[j]);
+                alpha[j] = fast_exp2(m_run[j] - mn);
+                m_run[j] = mn;
+                l_run[j] *= alpha[j];
+                z_run[j] *= alpha[j];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if constexpr (G == 4) {
+                    acc[i][0] *= alpha[0]; acc[i][1] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][3] *= alpha[0];
+                } else {
+                    acc[i][0] *= alpha[0]; acc[i][2] *= alpha[0]; acc[i][1] *= alpha[1]; acc[i][3] *= alpha[1];
+                }
+            }
+        }
+        // Sparse V: a row whose p (against the running reference max, never
+        // above the final max) is at most vthr keeps its softmax weight in l
+        // but adds nothing to the value sum; a 16-row tile with no such row
+        // left skips its value MMAs (SPARSE instantiations only).
+        float pp[2][NH][2];   // [row tile][head][row]: P' = p * v_scale
+        bool vlive[2] = {!SPARSE, !SPARSE};    // 16-row tiles that keep a row
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            float lsum = 0.f, zsum = 0.f;
+#pragma unroll
+            for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float p = fast_exp2(s[j][rt][r] - m_run[j]);   // 0 for masked rows
+                    lsum += p;
+                    if constexpr (SPARSE) {
+                        const bool keep = ok[rt][r] && p > a.vthr;
+                        vlive[rt] |= keep;
+                        zsum += keep ? p * vz[rt][r] : 0.f;
+                        pp[rt][j][r] = keep ? p * vs[rt][r] : 0.f;
+                    } else {
+                        zsum += ok[rt][r] ? p * vz[rt][r] : 0.f;
+                        pp[rt][j][r] = ok[rt][r] ? p * vs[rt][r] : 0.f;
+                    }
+                }
+            l_run[j] += lsum;
+            z_run[j] += zsum;
+        }
+
+        // ---- values
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+            if (SPARSE && !__any_sync(0xffffffffu, vlive[rt])) continue;   // warp-uniform
+            uint32_t pb[2][2];
+            p_to_b<G>(pp[rt], gid, tig, pb);
+            pv_tile<VBITS, G, KMODE == 8>(st + 16 * rt * rs + a.g.v_off, rs, gid, tig, vmis, pb, acc);
+        }
+    };
+
+    int failed_at = -1;
+    int stage = 0;               // it mod NST
+    uint32_t parity = 0;         // (it / NST) mod 2
+    for (int it = 0; it < ntiles; ++it) {
+        // tile `it` has landed; a copy that never completes ends this warp's
+        // heads with a NaN lse instead of hanging (bounded wait)
+        const bool ok_wait = mbar_wait(&full[stage], parity, kWaitLimit);
+        if (!__all_sync(0xffffffffu, ok_wait)) { failed_at = it; break; }
+        const uint8_t* st = smem + stage * stage_bytes + hoff;
+        const uint8_t* sm = smem + stage * stage_bytes + moff;
+        const int t0 = t_begin + it * kTile;
+        if (t0 + kTile <= t_end) tile(st, sm, t0, std::false_type{});
+        else                     tile(st, sm, t0, std::true_type{});
+
+        // ---- this warp is done with the stage; the last warp refills it
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&done[stage], 1) == nwarps - 1;
+            if (last) done[stage] = 0;
+            __threadfence_block();
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST, stage);
+        if (++stage == NST) { stage = 0; parity ^= 1u; }
+    }
+    // stage 2 (a programmatic dependent launch) may start its launch now; it
+    // waits for this grid's completion before it reads the partials
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (failed_at >= 0) {
+        // let the copies that may still be in flight (tiles failed_at ..
+        // failed_at + NST - 1) land, with the same bounded wait, then mark
+        // this warp's heads as failed
+        for (int it = failed_at; it < min(ntiles, failed_at + NST); ++it)
+            mbar_wait(&full[it % NST], uint32_t((it / NST) & 1), kWaitLimit);
+        if (lane < Greal)
+            a.mid[(((long long)b * Hq + h * Greal + lane) * S + split) * (kHeadDim + 1) + kHeadDim] =
+                __int_as_float(0x7fc00000);
+        return;
+    }
+
+    // ---------------- epilogue: finish the row sums, write o_s and lse_s.
+    // The value accumulators hold 2^-9 of sum_t p_t v_scale_t code_t.
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+#pragma unroll
+        for (int m = 4; m < 32; m <<= 1) {
+            l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], m);
+            z_run[j] += __shfl_xor_sync(0xffffffffu, z_run[j], m);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+        const int g = G == 4 ? tig : 2 * tig + j;
+        if (g >= Greal) continue;
+        const int hq = h * Greal + g;
+        float* mp = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
+        const float inv = 1.f / l_run[j];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int d = 16 * gid + 2 * i;
+            float e, o;
+            if constexpr (G == 4) { e = acc[i][0] + acc[i][1]; o = acc[i][2] + acc[i][3]; }
+            else { e = j == 0 ? acc[i][0] : acc[i][1]; o = j == 0 ? acc[i][2] : acc[i][3]; }
+            mp[d] = (e * 512.f + z_run[j]) * inv;
+            mp[d + 1] = (o * 512.f + z_run[j]) * inv;
+        }
+        if (gid == 0) mp[kHeadDim] = (m_run[j] + log2f(l_run[j])) * 0.6931471805599453f;
+    }
+}
+
+template <typename TQ, int KMODE, int VBITS, int G, bool SPARSE>
+cudaError_t launch_t(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
+{
+    auto k = a.g.soa ? stage1_mma_kernel<TQ, KMODE, VBITS, G, true, SPARSE>
+                     : stage1_mma_kernel<TQ, KMODE, VBITS, G, false, SPARSE>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.num_splits, B, a.Hk / a.hpc);
+    k<<<grid, 32 * a.hpc, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename TQ, int KMODE, int VBITS, bool SPARSE>
+cudaError_t launch_g(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
+{
+    return a.G <= 4 ? launch_t<TQ, KMODE, VBITS, 4, SPARSE>(a, B, smem, st)
+                    : launch_t<TQ, KMODE, VBITS, 8, SPARSE>(a, B, smem, st);
+}
+
+template <typename TQ, bool SPARSE>
+cudaError_t launch_q(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
+{
+    if (a.g.key_fp8) return launch_g<TQ, 8, 4, SPARSE>(a, B, smem, st);
+    if (a.g.key_bits == 4) return launch_g<TQ, 4, 4, SPARSE>(a, B, smem, st);
+    if (a.g.key_bits == 2) return launch_g<TQ, 2, 2, SPARSE>(a, B, smem, st);
+    if (a.g.value_bits == 4) return launch_g<TQ, 3, 4, SPARSE>(a, B, smem, st);
+    return launch_g<TQ, 3, 3, SPARSE>(a, B, smem, st);
+}
+
+}  // namespace
+}  // namespace tq
