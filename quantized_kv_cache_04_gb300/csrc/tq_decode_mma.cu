@@ -34,13 +34,15 @@ MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G)
     // warp reads in the same instruction on distinct bank quads
     m.smem_row = (m.copy_bytes % 32 == 0) ? m.copy_bytes + 16 : m.copy_bytes;
     const int stage = kTile * (m.smem_row + m.meta_bytes);
-    // ring budget: two CTAs of Hk warps, or four CTAs of 4 warps, per SM
-    int nst = (m.hpc < Hk ? 56 * 1024 : 100 * 1024) / stage;
+    // ring budget: two CTAs of Hk warps, or four CTAs of 4 warps, per SM;
+    // MSE keys with G = 8 also keep 4 KB of q fragments per warp
+    const int qsm = (!L.key_fp8 && G > 4) ? m.hpc * 4096 : 0;
+    int nst = ((m.hpc < Hk ? 56 * 1024 : 100 * 1024) + (qsm ? 12 * 1024 : 0) - qsm) / stage;
     nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
     // the q staging at kernel start borrows the ring: hpc * (4 or 8) heads * 512 B
     while (nst * stage < m.hpc * (G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
     m.nstages = nst;
-    m.smem = size_t(nst) * stage + 16 * size_t(nst);   // ring + mbarrier and counter per stage
+    m.smem = size_t(nst) * stage + 16 * size_t(nst) + size_t(qsm);   // ring, mbarrier + counter per stage, q
     return m;
 }
 

@@ -232,10 +232,13 @@ __device__ __forceinline__ void lut16(const uint32_t (&T)[8][2], uint32_t s, uin
 
 // Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1: row gid+8).
 // Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
+// MSE keys with G = 8 read their q fragments from shared memory (qsm: this
+// lane's uint4 of k-step 0, stride 32).
 template <int KMODE, int G, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
-                                        const uint32_t (&T)[NT][2], float (&out)[4], float (&outl)[4])
+                                        const uint4* qsm, const uint32_t (&T)[NT][2], float (&out)[4],
+                                        float (&outl)[4])
 {
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float scl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -306,9 +309,10 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
                 mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
                 mma16816(sc[1], Alo, bq[kk][0], bq[kk][1]);
             } else {
-                mma16816(sc[kk & 1], Ahi, bq[kk][0], bq[kk][1]);
-                mma16816(scl[0], Ahi, bql[kk][0], bql[kk][1]);
-                mma16816(scl[1], Alo, bq[kk][0], bq[kk][1]);
+                const uint4 qf = qsm[32 * kk];      // q hi (x, y) and lo (z, w) of this k-step
+                mma16816(sc[kk & 1], Ahi, qf.x, qf.y);
+                mma16816(scl[0], Ahi, qf.z, qf.w);
+                mma16816(scl[1], Alo, qf.x, qf.y);
             }
         }
     }
@@ -552,6 +556,11 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     //   4-bit keys: the same, 16 bytes per thread
     //   2-bit keys: 32 tig + 16 (kk >> 2) + 8 (kk & 1) + ((kk >> 1) & 1) + 2 j
     //               (8 bytes per thread; see qk_tile)
+    // MSE keys with G = 8 keep their q fragments in shared memory after the
+    // ring's barriers (4 KB per warp, read once per k-step) instead of 32
+    // registers: the register file is the limit of that instantiation.
+    constexpr bool kQsm = KMODE != 8 && G == 8;
+    uint4* qsm = reinterpret_cast<uint4*>(smem + NST * stage_bytes + 16 * NST) + warp * 256 + lane;
     uint32_t bq[8][2], bql[8][2];
     {
         float* sq = reinterpret_cast<float*>(smem + q_base) + warp * G * kHeadDim;
@@ -603,6 +612,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
                 bq[kk][1] = pack_half2(hi[2], hi[3]);
                 bql[kk][0] = pack_half2(lo[0], lo[1]);
                 bql[kk][1] = pack_half2(lo[2], lo[3]);
+                if constexpr (kQsm) {
+                    qsm[32 * kk] = make_uint4(bq[kk][0], bq[kk][1], bql[kk][0], bql[kk][1]);
+                    bq[kk][0] = bq[kk][1] = bql[kk][0] = bql[kk][1] = 0u;
+                }
             }
         }
         __syncthreads();            // every warp is done with the staging area
@@ -665,7 +678,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
-            qk_tile<KMODE, G>(r0, r1, tig, kmis, bq, bql, T, sc, scl);
+            qk_tile<KMODE, G>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
             float n0 = 1.f, n1 = 1.f;
             if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
             vs[rt][0] = lds_f16(m0 + a.g.m_scale);

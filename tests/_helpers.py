@@ -89,14 +89,15 @@ def check_decode(out, lse, ref_out, ref_lse, what=""):
     return mx, rel
 
 
-def paged_problem(orc, preset, seq_lens, Hk, bs, rng, dtype="float16", kscale=1.0):
+def paged_problem(orc, preset, seq_lens, Hk, bs, rng, dtype="float16", kscale=1.0, book=None):
     """Random paged cache built by the ORACLE (fp16/bf16-exact inputs).
+    `book`: (centroids, midpoints) to use instead of the Lloyd-Max codebook.
     Returns dict with cache (with a 0xFF guard block), block_table, K, V."""
     import torch
     D = 128
     L = orc.layout(preset)
     s = orc.signs(D, 42)
-    c32, m32 = codebook(orc, preset)
+    c32, m32 = codebook(orc, preset) if book is None else book
     nblk = [(int(n) + bs - 1) // bs for n in seq_lens]
     total = sum(nblk)
     perm = rng.permutation(total)

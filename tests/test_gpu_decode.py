@@ -91,6 +91,26 @@ def test_decode_on_oracle_cache(orc, preset, case, qdtype):
     assert np.all(np.abs(o16 - ref16) <= ulp * 1.0001 + 2e-5)
 
 
+@pytest.mark.parametrize("preset", [1, 2, 3, 4])
+@pytest.mark.parametrize("G,Hk,bs,seq_lens", [(4, 8, 16, [300, 77]), (8, 8, 64, [400]),
+                                              (4, 2, 32, [129])])
+def test_decode_custom_codebook(orc, preset, G, Hk, bs, seq_lens):
+    """A codebook other than the library's Lloyd-Max one (entries moved by up
+    to 2%, no longer symmetric): the decode picks its own centroid scale for
+    the fp16 + E4M3 score split and still meets the tolerances."""
+    L = orc.layout(preset)
+    rng = np.random.default_rng(4200 + 10 * preset + G)
+    c, _ = codebook(orc, preset)
+    c = np.sort(c.astype(np.float64) * (1.0 + 0.02 * rng.uniform(-1, 1, c.shape))).astype(np.float32)
+    m = ((c[1:].astype(np.float64) + c[:-1]) / 2).astype(np.float32)
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng, book=(c, m))
+    q = torch.from_numpy(rng.normal(size=(len(seq_lens), G * Hk, 128)) * 2.0).to(torch.float16)
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], pb["bt"],
+                                    np.asarray(seq_lens, np.int32), Hk, bs, pb["signs"], c)
+    o, l = _gpu_decode(preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"], c)
+    check_decode(o, l, ref_o, ref_l, f"preset {preset} custom codebook")
+
+
 @pytest.mark.parametrize("preset", PRESETS)
 def test_split_count_invariance(orc, preset):
     """Results do not depend on the split count beyond rounding."""
