@@ -128,6 +128,7 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
     a.meta_bytes = m.meta_bytes;
     a.nstages = m.nstages;
     a.g = geom_of(L, soa);
+    a.lpt = (B <= 512 && m.smem >= size_t(4) * (B + 1)) ? 1 : 0;
     const cudaError_t e = v_threshold > 0.f ? launch_mma_sparse(a, q_dtype, B, m.smem, st)
                                             : launch_mma_dense(a, q_dtype, B, m.smem, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

@@ -52,6 +52,7 @@ struct MmaArgs {
     int meta_bytes;          // SoA: hpc * metadata record per token (0 for AoS)
     int nstages;
     float vthr;              // sparse V: rows with p <= vthr skip the value sum (0: off)
+    int lpt;                 // 1: CTA row y takes the y-th longest sequence (seq_of_rank)
     SlotGeom g;
 };
 
@@ -171,6 +172,30 @@ __device__ __forceinline__ void nibbles3(const uint32_t (&w)[3], uint32_t (&n)[4
     n[1] = w[1] & 0x77777777u;
     n[2] = w[2] & 0x77777777u;
     n[3] = ((w[0] >> 3) & 0x11111111u) | ((w[1] >> 2) & 0x22222222u) | ((w[2] >> 1) & 0x44444444u);
+}
+
+// Longest-first dispatch: CTA row y (blockIdx.y) takes the sequence of rank y
+// when the batch is ordered by decreasing length (ties by index), so the
+// block scheduler starts the longest sequences' splits first and the short
+// ones fill the tail of the grid.  O(B) per thread for B <= 512; `sl` is
+// (B + 1) ints of shared memory; all threads of the block call it.
+__device__ __forceinline__ int seq_of_rank(const int32_t* seq_lens, int B, int r, int* sl)
+{
+    for (int i = threadIdx.x; i < B; i += blockDim.x) sl[i] = seq_lens[i];
+    __syncthreads();
+    for (int c = threadIdx.x; c < B; c += blockDim.x) {
+        const int Lc = sl[c];
+        int rank = 0;
+        for (int j = 0; j < B; ++j) {
+            const int Lj = sl[j];
+            rank += (Lj > Lc) || (Lj == Lc && j < c);
+        }
+        if (rank == r) sl[B] = c;        // the ranks are a permutation: one writer
+    }
+    __syncthreads();
+    const int b = sl[B];
+    __syncthreads();                     // the area is reused afterwards
+    return b;
 }
 
 // Token of QK row r (0..15) inside a tile.  Rows r and r+8 of a thread hold
@@ -450,7 +475,9 @@ template <typename TQ, int KMODE, int VBITS, int G, bool SOA, bool SPARSE>
 __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int split = blockIdx.x, b = blockIdx.y;
+    const int split = blockIdx.x;
+    const int b = a.lpt ? seq_of_rank(a.seq_lens, gridDim.y, blockIdx.y, reinterpret_cast<int*>(smem))
+                        : blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int h0 = blockIdx.z * a.hpc;        // first kv head of this CTA
