@@ -446,23 +446,23 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
                 if constexpr (G == 8) mma16816(acc[i + u], A[u], pb[1][0], pb[1][1]);
             }
         }
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-        const uint32_t c = uint32_t(i & 3);
-        const uint32_t sel = c | ((c + 4) << 4) | ((c + 1) << 8) | ((c + 5) << 12);
-        const uint32_t ab = prmt(vw[0][i >> 2], vw[1][i >> 2], sel);
-        const uint32_t cd = prmt(vw[2][i >> 2], vw[3][i >> 2], sel);
-        uint32_t A0[4], A1[4];
-        cvt_e4m3x4(ab & 0x0F0F0F0Fu, A0[0], A1[0]);
-        cvt_e4m3x4((ab >> 4) & 0x0F0F0F0Fu, A0[1], A1[1]);
-        cvt_e4m3x4(cd & 0x0F0F0F0Fu, A0[2], A1[2]);
-        cvt_e4m3x4((cd >> 4) & 0x0F0F0F0Fu, A0[3], A1[3]);
-        mma16816(acc[i], A0, pb[0][0], pb[0][1]);
-        if constexpr (G == 8) mma16816(acc[i], A0, pb[1][0], pb[1][1]);
-        mma16816(acc[i + 1], A1, pb[0][0], pb[0][1]);
-        if constexpr (G == 8) mma16816(acc[i + 1], A1, pb[1][0], pb[1][1]);
+        for (int i = 0; i < 8; i += 2) {
+            const uint32_t c = uint32_t(i & 3);
+            const uint32_t sel = c | ((c + 4) << 4) | ((c + 1) << 8) | ((c + 5) << 12);
+            const uint32_t ab = prmt(vw[0][i >> 2], vw[1][i >> 2], sel);
+            const uint32_t cd = prmt(vw[2][i >> 2], vw[3][i >> 2], sel);
+            uint32_t A0[4], A1[4];
+            cvt_e4m3x4(ab & 0x0F0F0F0Fu, A0[0], A1[0]);
+            cvt_e4m3x4((ab >> 4) & 0x0F0F0F0Fu, A0[1], A1[1]);
+            cvt_e4m3x4(cd & 0x0F0F0F0Fu, A0[2], A1[2]);
+            cvt_e4m3x4((cd >> 4) & 0x0F0F0F0Fu, A0[3], A1[3]);
+            mma16816(acc[i], A0, pb[0][0], pb[0][1]);
+            if constexpr (G == 8) mma16816(acc[i], A0, pb[1][0], pb[1][1]);
+            mma16816(acc[i + 1], A1, pb[0][0], pb[0][1]);
+            if constexpr (G == 8) mma16816(acc[i + 1], A1, pb[1][0], pb[1][1]);
+        }
     }
 }
 
@@ -475,6 +475,10 @@ template <typename TQ, int KMODE, int VBITS, int G, bool SOA, bool SPARSE>
 __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
+    // launched as a programmatic dependent of the previous kernel in the
+    // stream (typically the store of the step's new tokens): wait for it to
+    // complete before the first read of global memory
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int split = blockIdx.x;
     const int b = a.lpt ? seq_of_rank(a.seq_lens, gridDim.y, blockIdx.y, reinterpret_cast<int*>(smem))
                         : blockIdx.y;
@@ -886,9 +890,17 @@ cudaError_t launch_t(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
                      : stage1_mma_kernel<TQ, KMODE, VBITS, G, false, SPARSE>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(a.num_splits, B, a.Hk / a.hpc);
-    k<<<grid, 32 * a.hpc, smem, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_splits, B, a.Hk / a.hpc);
+    cfg.blockDim = dim3(32 * a.hpc);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 template <typename TQ, int KMODE, int VBITS, bool SPARSE>

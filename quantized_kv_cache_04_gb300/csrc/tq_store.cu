@@ -79,6 +79,9 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float s_cent[16], s_mid[16];
+    // a decode launched next as a programmatic dependent may start its
+    // prologue now; it waits for this grid's completion before reading memory
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
     const int S = a.g.slot;
     const int row_bytes = a.num_kv_heads * S;
