@@ -223,59 +223,95 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
     }
 }
 
-// Stage 2: one warp per (sequence, query head).  Lanes take the splits' LSEs
-// for the max and the weight sum; then each lane owns 4 of the 128 dims and
-// accumulates the weighted split outputs (independent loads across splits).
-constexpr int kStage2Warps = 4;
+// Stage 2: the log-sum-exp merge of the split partials.  A row (sequence,
+// query head) takes R = ceil(S / 16) warps (at most 8), each merging every
+// R-th split in rounds of 16 with every load of a round issued before any
+// arithmetic; lane l owns dims 4l..4l+3.  The R partial merges (running max
+// M, weight sum W, weighted output) are combined through shared memory by
+// the row's first warp.  A NaN lse (a split that gave up waiting for its
+// data) makes the row NaN.
+constexpr int kStage2Warps = 8;
 
 template <typename TO>
-__global__ void __launch_bounds__(32 * kStage2Warps) stage2_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(32 * kStage2Warps) stage2_kernel(DecodeArgs a, int R)
 {
+    __shared__ float s_part[kStage2Warps][kHeadDim + 2];
     // launched as a programmatic dependent of stage 1: wait until its
     // partials are complete and visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int lane = threadIdx.x & 31;
-    const long long bh = (long long)blockIdx.x * kStage2Warps + (threadIdx.x >> 5);   // b * Hq + hq
-    if (bh >= (long long)a.B * a.Hq) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rows_per_cta = kStage2Warps / R;
+    const int r = warp % R;                                    // this warp's share of the splits
+    const long long bh = (long long)blockIdx.x * rows_per_cta + warp / R;   // b * Hq + hq
+    const bool live = bh < (long long)a.B * a.Hq;
     const int S = a.num_splits;
-    const float* mp = a.mid + bh * S * (kHeadDim + 1);
-    // One pass over the splits in rounds of kRound: every load of a round is
-    // issued before any arithmetic, and the running max M moves by rescaling
-    // (the log-sum-exp merge of the split partials).  A NaN lse (a split
-    // that gave up waiting for its data) makes the row NaN.
     constexpr int kRound = 16;
     float M = -INFINITY, W = 0.f;
     float o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s0 = 0; s0 < S; s0 += kRound) {
-        float ls[kRound], x[kRound][4];
+    if (live) {
+        const float* mp = a.mid + bh * S * (kHeadDim + 1);
+        for (int s0 = r; s0 < S; s0 += kRound * R) {
+            float ls[kRound], x[kRound][4];
 #pragma unroll
-        for (int u = 0; u < kRound; ++u) {
-            const float* row = mp + min(s0 + u, S - 1) * (kHeadDim + 1);
-            ls[u] = s0 + u < S ? row[kHeadDim] : -INFINITY;
+            for (int u = 0; u < kRound; ++u) {
+                const int sp = s0 + u * R;
+                const float* row = mp + min(sp, S - 1) * (kHeadDim + 1);
+                ls[u] = sp < S ? row[kHeadDim] : -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[u][i] = row[4 * lane + i];
+                for (int i = 0; i < 4; ++i) x[u][i] = row[4 * lane + i];
+            }
+            float mc = M;
+            bool nan = false;
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) { mc = fmaxf(mc, ls[u]); nan |= ls[u] != ls[u]; }
+            if (nan) { M = W = __int_as_float(0x7fc00000); break; }
+            if (mc == -INFINITY) continue;            // only empty splits so far
+            const float sc = expf(M - mc);            // 0 while M = -inf
+            W *= sc;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] *= sc;
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                const float w = expf(ls[u] - mc);     // 0 for empty and padding splits
+                W += w;
+                if (w != 0.f) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] += w * x[u][i];
+                }
+            }
+            M = mc;
         }
-        float mc = M;
+    }
+    if (R > 1) {                                     // uniform per launch
+        float* sp = s_part[warp];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sp[4 * lane + i] = o[i];
+        if (lane == 0) { sp[kHeadDim] = M; sp[kHeadDim + 1] = W; }
+        __syncthreads();
+        if (r != 0) return;
+        M = -INFINITY;
         bool nan = false;
+        for (int j = 0; j < R; ++j) {
+            const float mj = s_part[warp + j][kHeadDim];
+            nan |= mj != mj;
+            M = fmaxf(M, mj);
+        }
+        W = 0.f;
 #pragma unroll
-        for (int u = 0; u < kRound; ++u) { mc = fmaxf(mc, ls[u]); nan |= ls[u] != ls[u]; }
-        if (nan) { M = W = __int_as_float(0x7fc00000); break; }
-        if (mc == -INFINITY) continue;            // only empty splits so far
-        const float sc = expf(M - mc);            // 0 while M = -inf
-        W *= sc;
+        for (int i = 0; i < 4; ++i) o[i] = 0.f;
+        if (nan) {
+            M = W = __int_as_float(0x7fc00000);
+        } else if (M != -INFINITY) {
+            for (int j = 0; j < R; ++j) {
+                const float* pj = s_part[warp + j];
+                const float f = pj[kHeadDim] == -INFINITY ? 0.f : expf(pj[kHeadDim] - M);
+                W += pj[kHeadDim + 1] * f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] *= sc;
-#pragma unroll
-        for (int u = 0; u < kRound; ++u) {
-            const float w = expf(ls[u] - mc);     // 0 for empty and padding splits
-            W += w;
-            if (w != 0.f) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) o[i] += w * x[u][i];
+                for (int i = 0; i < 4; ++i) o[i] += pj[4 * lane + i] * f;
             }
         }
-        M = mc;
     }
+    if (!live) return;
     if (M != -INFINITY) {
         const float inv = 1.f / W;
 #pragma unroll
@@ -290,9 +326,11 @@ __global__ void __launch_bounds__(32 * kStage2Warps) stage2_kernel(DecodeArgs a)
 template <typename TO>
 cudaError_t launch_stage2(const DecodeArgs& a, cudaStream_t st)
 {
-    const unsigned rows = unsigned(a.B) * a.Hq;
+    int R = (a.num_splits + 15) / 16;                 // warps per row: at most 16 splits each
+    R = R <= 1 ? 1 : R <= 2 ? 2 : R <= 4 ? 4 : 8;     // a divisor of kStage2Warps
+    const unsigned rows = unsigned(a.B) * a.Hq, rows_per_cta = kStage2Warps / R;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((rows + kStage2Warps - 1) / kStage2Warps);
+    cfg.gridDim = dim3((rows + rows_per_cta - 1) / rows_per_cta);
     cfg.blockDim = dim3(32 * kStage2Warps);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -301,7 +339,7 @@ cudaError_t launch_stage2(const DecodeArgs& a, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stage2_kernel<TO>, a);
+    return cudaLaunchKernelEx(&cfg, stage2_kernel<TO>, a, R);
 }
 
 template <typename TQ, bool FP8, int KB, int VB>
