@@ -2,6 +2,9 @@
 // dense instantiations (the kernel itself is in tq_decode_mma.cuh).
 #include "tq_decode_mma.cuh"
 
+#include <array>
+#include <cmath>
+
 namespace tq {
 
 cudaError_t launch_mma_dense(const MmaArgs& a, int q_dtype, int B, size_t smem, cudaStream_t st)
@@ -11,6 +14,60 @@ cudaError_t launch_mma_dense(const MmaArgs& a, int q_dtype, int B, size_t smem, 
 }
 
 namespace {
+
+// ---- 2-bit keys: a centroid scale alpha in [1, 2) with every alpha * c_k
+// of the library's codebook (two magnitudes) an fp16 value to ~1e-7
+// relative, so the score MMAs need no lo part.  Searched once per process
+// on the host, rounding like the device (the fp32 product, then
+// nearest-even fp16); candidates make one entry exact, plus a uniform grid.
+// The kernel checks the result against the centroids it is given.
+double round_f16(double x)
+{
+    if (x == 0.0) return 0.0;
+    int e;
+    const double m = std::frexp(x, &e);              // |m| in [0.5, 1)
+    if (e - 1 < -14) return std::nearbyint(x * 16777216.0) / 16777216.0;   // subnormal: 2^-24 steps
+    return std::ldexp(std::nearbyint(std::ldexp(m, 11)), e - 11);
+}
+
+double hi_error(const float* c, int n, float alpha)
+{
+    double err = 0.0;
+    for (int k = 0; k < n; ++k) {
+        const double x = double(alpha * c[k]);
+        const double d = std::fabs(x - round_f16(x));
+        err = std::fmax(err, x != 0.0 ? d / std::fabs(x) : d);
+    }
+    return err;
+}
+
+float two_bit_alpha()
+{
+    static const float alpha = [] {
+        float c[4], mid[4];
+        if (tq_build_codebook(kHeadDim, 2, c, mid) != TQ_OK) return 0.f;
+        double best = INFINITY;
+        float best_a = 0.f;
+        auto consider = [&](double g) {
+            const float a = float(g);
+            if (!(a >= 1.f && a < 2.f)) return;
+            const double e = hi_error(c, 4, a);
+            if (e < best || (e == best && a < best_a)) { best = e; best_a = a; }
+        };
+        for (int k = 0; k < 4; ++k) {
+            int e;
+            const double f = 2.0 * std::frexp(std::fabs(double(c[k])), &e);   // in [1, 2)
+            if (!(f >= 1.0)) continue;
+            for (int m = 0; m < 1024; ++m) {
+                double g = (1.0 + m / 1024.0) / f;
+                consider(g < 1.0 ? 2.0 * g : g);
+            }
+        }
+        for (int i = 0; i < 65536; ++i) consider(1.0 + i / 65536.0);
+        return best <= 5e-7 ? best_a : 0.f;
+    }();
+    return alpha;
+}
 
 // Launch geometry shared by the launcher and the occupancy query.
 struct MmaGeom {
@@ -105,6 +162,7 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
 {
     MmaArgs a;
     a.vthr = v_threshold;
+    a.key_alpha = (!L.key_fp8 && L.key_bits == 2) ? two_bit_alpha() : 0.f;
     a.query = query;
     a.cache = kv_cache;
     a.block_table = block_table;

@@ -53,6 +53,7 @@ struct MmaArgs {
     int nstages;
     float vthr;              // sparse V: rows with p <= vthr skip the value sum (0: off)
     int lpt;                 // 1: CTA row y takes the y-th longest sequence (seq_of_rank)
+    float key_alpha;         // 2-bit keys: centroid scale making alpha * c_k fp16-exact (0: none)
     SlotGeom g;
 };
 
@@ -259,7 +260,7 @@ __device__ __forceinline__ void lut16(const uint32_t (&T)[8][2], uint32_t s, uin
 // Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
 // MSE keys with G = 8 read their q fragments from shared memory (qsm: this
 // lane's uint4 of k-step 0, stride 32).
-template <int KMODE, int G, int NT>
+template <int KMODE, int G, bool LO, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
                                         const uint4* qsm, const uint32_t (&T)[NT][2], float (&out)[4],
@@ -310,7 +311,8 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t s0 = c0[kk >> 1] >> (16 * (kk & 1));
             const uint32_t s1 = c1[kk >> 1] >> (16 * (kk & 1));
-            uint32_t Ahi[4], Alo[4];
+            uint32_t Ahi[4], Alo[4] = {0u, 0u, 0u, 0u};
+            constexpr bool use_lo = KMODE != 2 || LO;   // 2-bit keys may need no lo part
             if constexpr (KMODE == 4) {
                 lut16(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
                 lut16(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
@@ -323,21 +325,27 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
                 Ahi[2] = prmt(p0, p1, 0x7362u);
                 Ahi[1] = prmt(q0, q1, 0x5140u);
                 Ahi[3] = prmt(q0, q1, 0x7362u);
-                const uint32_t u0 = prmt(T[2][0], T[2][1], s0), u1 = prmt(T[3][0], T[3][1], s0);
-                const uint32_t v0 = prmt(T[2][0], T[2][1], s1), v1 = prmt(T[3][0], T[3][1], s1);
-                Alo[0] = prmt(u0, u1, 0x5140u);
-                Alo[2] = prmt(u0, u1, 0x7362u);
-                Alo[1] = prmt(v0, v1, 0x5140u);
-                Alo[3] = prmt(v0, v1, 0x7362u);
+                if constexpr (use_lo) {
+                    const uint32_t u0 = prmt(T[2][0], T[2][1], s0), u1 = prmt(T[3][0], T[3][1], s0);
+                    const uint32_t v0 = prmt(T[2][0], T[2][1], s1), v1 = prmt(T[3][0], T[3][1], s1);
+                    Alo[0] = prmt(u0, u1, 0x5140u);
+                    Alo[2] = prmt(u0, u1, 0x7362u);
+                    Alo[1] = prmt(v0, v1, 0x5140u);
+                    Alo[3] = prmt(v0, v1, 0x7362u);
+                }
             }
             if constexpr (G == 4) {
-                mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
-                mma16816(sc[1], Alo, bq[kk][0], bq[kk][1]);
+                if constexpr (use_lo) {
+                    mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
+                    mma16816(sc[1], Alo, bq[kk][0], bq[kk][1]);
+                } else {
+                    mma16816(sc[kk & 1], Ahi, bq[kk][0], bq[kk][1]);
+                }
             } else {
                 const uint4 qf = qsm[32 * kk];      // q hi (x, y) and lo (z, w) of this k-step
                 mma16816(sc[kk & 1], Ahi, qf.x, qf.y);
                 mma16816(scl[0], Ahi, qf.z, qf.w);
-                mma16816(scl[1], Alo, qf.x, qf.y);
+                if constexpr (use_lo) mma16816(scl[1], Alo, qf.x, qf.y);
             }
         }
     }
@@ -587,6 +595,24 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     //   4-bit keys: the same, 16 bytes per thread
     //   2-bit keys: 32 tig + 16 (kk >> 2) + 8 (kk & 1) + ((kk >> 1) & 1) + 2 j
     //               (8 bytes per thread; see qk_tile)
+    // 2-bit keys: the host passes a scale alpha that makes every alpha * c_k
+    // of the library's codebook an fp16 value to 5e-7 relative.  If that holds
+    // for the centroids given (the same test in every thread), the keys use
+    // fp16(alpha c_k) alone and q carries 1 / alpha: no lo lookups or MMAs.
+    float key_alpha = 1.f;
+    bool key_lo = KMODE != 8;
+    if constexpr (KMODE == 2) {
+        const float al = a.key_alpha;
+        float err = (al >= 1.f && al < 2.f) ? 0.f : INFINITY;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float x = al * a.centroids[k];
+            const float d = fabsf(x - __half2float(__float2half_rn(x)));
+            err = fmaxf(err, x != 0.f ? d / fabsf(x) : d);
+        }
+        if (err <= 5e-7f) { key_alpha = al; key_lo = false; }
+    }
+
     // MSE keys with G = 8 keep their q fragments in shared memory after the
     // ring's barriers (4 KB per warp, read once per k-step) instead of 32
     // registers: the register file is the limit of that instantiation.
@@ -611,7 +637,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
                     for (int i = 0; i < 4; ++i) qv[i] *= 0.08838834764831845f;
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) qv[i] *= a.qscale;
+                for (int i = 0; i < 4; ++i) qv[i] *= a.qscale / key_alpha;
             }
             reinterpret_cast<float4*>(sq + g * kHeadDim)[lane] = make_float4(qv[0], qv[1], qv[2], qv[3]);
         }
@@ -656,7 +682,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 
     // ---------------- centroid byte planes for the PRMT lookup (MSE keys):
     // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
-    // fp16 residual c - fp16(c).  2- and 3-bit keys: T[p][k >> 2] holds entries
+    // fp16 residual c - fp16(c), with c = key_alpha * c_k.  2- and 3-bit keys: T[p][k >> 2] holds entries
     // 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
     // plane p of codes 8(k>>3) .. 8(k>>3)+7 in the same way.
     uint32_t T[KMODE == 4 ? 8 : 4][2] = {};
@@ -664,7 +690,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         constexpr int NC = 1 << KMODE;
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
-            const float c = a.centroids[k];
+            const float c = key_alpha * a.centroids[k];
             const __half chi = __float2half_rn(c);
             const __half clo = __float2half_rn(c - __half2float(chi));
             const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
@@ -697,8 +723,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 
     // One 32-token tile in stage memory st (this warp's slot at offset 0).
     // PARTIAL: some of its tokens lie at or past t_end and are masked.
-    auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag) {
+    // LO: the keys' lo part is needed (all but 2-bit keys with key_alpha)
+    auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag, auto lo_tag) {
         constexpr bool PARTIAL = decltype(partial_tag)::value;
+        constexpr bool LO = decltype(lo_tag)::value;
         // ---- scores of both 16-row tiles
         float s[NH][2][2], vs[2][2], vz[2][2];
         bool ok[2][2];
@@ -709,7 +737,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
-            qk_tile<KMODE, G>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
+            qk_tile<KMODE, G, LO>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
             float n0 = 1.f, n1 = 1.f;
             if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
             vs[rt][0] = lds_f16(m0 + a.g.m_scale);
@@ -812,32 +840,39 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
     };
 
-    int failed_at = -1;
-    int stage = 0;               // it mod NST
-    uint32_t parity = 0;         // (it / NST) mod 2
-    for (int it = 0; it < ntiles; ++it) {
-        // tile `it` has landed; a copy that never completes ends this warp's
-        // heads with a NaN lse instead of hanging (bounded wait)
-        const bool ok_wait = mbar_wait(&full[stage], parity, kWaitLimit);
-        if (!__all_sync(0xffffffffu, ok_wait)) { failed_at = it; break; }
-        const uint8_t* st = smem + stage * stage_bytes + hoff;
-        const uint8_t* sm = smem + stage * stage_bytes + moff;
-        const int t0 = t_begin + it * kTile;
-        if (t0 + kTile <= t_end) tile(st, sm, t0, std::false_type{});
-        else                     tile(st, sm, t0, std::true_type{});
+    // The tile loop; returns the tile whose wait gave up, or -1.  2-bit keys
+    // instantiate it with and without the lo part and pick once per CTA.
+    auto run = [&](auto lo_tag) {
+        int stage = 0;               // it mod NST
+        uint32_t parity = 0;         // (it / NST) mod 2
+        for (int it = 0; it < ntiles; ++it) {
+            // tile `it` has landed; a copy that never completes ends this warp's
+            // heads with a NaN lse instead of hanging (bounded wait)
+            const bool ok_wait = mbar_wait(&full[stage], parity, kWaitLimit);
+            if (!__all_sync(0xffffffffu, ok_wait)) return it;
+            const uint8_t* st = smem + stage * stage_bytes + hoff;
+            const uint8_t* sm = smem + stage * stage_bytes + moff;
+            const int t0 = t_begin + it * kTile;
+            if (t0 + kTile <= t_end) tile(st, sm, t0, std::false_type{}, lo_tag);
+            else                     tile(st, sm, t0, std::true_type{}, lo_tag);
 
-        // ---- this warp is done with the stage; the last warp refills it
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            last = atomicAdd(&done[stage], 1) == nwarps - 1;
-            if (last) done[stage] = 0;
-            __threadfence_block();
+            // ---- this warp is done with the stage; the last warp refills it
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&done[stage], 1) == nwarps - 1;
+                if (last) done[stage] = 0;
+                __threadfence_block();
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST, stage);
+            if (++stage == NST) { stage = 0; parity ^= 1u; }
         }
-        if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST, stage);
-        if (++stage == NST) { stage = 0; parity ^= 1u; }
-    }
+        return -1;
+    };
+    int failed_at;
+    if constexpr (KMODE == 2) failed_at = key_lo ? run(std::true_type{}) : run(std::false_type{});
+    else                      failed_at = run(std::true_type{});
     // stage 2 (a programmatic dependent launch) may start its launch now; it
     // waits for this grid's completion before it reads the partials
     asm volatile("griddepcontrol.launch_dependents;");
