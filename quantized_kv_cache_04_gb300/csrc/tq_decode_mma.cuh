@@ -142,11 +142,13 @@ __device__ __forceinline__ void fence_async_shared()
 }
 
 // n little-endian 32-bit words starting at the 2-byte aligned shared address p.
-// `mis` (0 or 2, uniform per warp) is p mod 4; ALIGNED promises mis == 0.
-template <int N, bool ALIGNED = false>
+// `mis` (0 or 2, uniform per warp) is p mod 4.  MIS = 0 or 2 fixes it at
+// compile time (the tile loop is instantiated per warp misalignment: a
+// branch in the loop costs more than the loads); MIS = -1 reads `mis`.
+template <int N, int MIS = -1>
 __device__ __forceinline__ void lds_words(const uint8_t* p, int mis, uint32_t (&w)[N])
 {
-    if (ALIGNED || mis == 0) {
+    if (MIS == 0 || (MIS < 0 && mis == 0)) {
         const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
 #pragma unroll
         for (int i = 0; i < N; ++i) w[i] = q[i];
@@ -260,7 +262,7 @@ __device__ __forceinline__ void lut16(const uint32_t (&T)[8][2], uint32_t s, uin
 // Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
 // MSE keys with G = 8 read their q fragments from shared memory (qsm: this
 // lane's uint4 of k-step 0, stride 32).
-template <int KMODE, int G, bool LO, int NT>
+template <int KMODE, int G, bool LO, int KM, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
                                         const uint4* qsm, const uint32_t (&T)[NT][2], float (&out)[4],
@@ -285,8 +287,8 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
         uint32_t c0[4], c1[4];
         if constexpr (KMODE == 3) {
             uint32_t w0[3], w1[3];
-            lds_words<3>(r0 + 12 * tig, kmis, w0);
-            lds_words<3>(r1 + 12 * tig, kmis, w1);
+            lds_words<3, KM>(r0 + 12 * tig, kmis, w0);
+            lds_words<3, KM>(r1 + 12 * tig, kmis, w1);
             nibbles3(w0, c0);
             nibbles3(w1, c1);
         } else if constexpr (KMODE == 2) {
@@ -294,8 +296,8 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
             // nibble word and the odd codes to another (code 2i / 2i + 1 of
             // the word in nibble i), so k-step kk covers dims with stride 2
             uint32_t w0[2], w1[2];
-            lds_words<2>(r0 + 8 * tig, kmis, w0);
-            lds_words<2>(r1 + 8 * tig, kmis, w1);
+            lds_words<2, KM>(r0 + 8 * tig, kmis, w0);
+            lds_words<2, KM>(r1 + 8 * tig, kmis, w1);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 c0[2 * i] = w0[i] & 0x33333333u;
@@ -304,8 +306,8 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
                 c1[2 * i + 1] = (w1[i] >> 2) & 0x33333333u;
             }
         } else {
-            lds_words<4>(r0 + 16 * tig, kmis, c0);
-            lds_words<4>(r1 + 16 * tig, kmis, c1);
+            lds_words<4, KM>(r0 + 16 * tig, kmis, c0);
+            lds_words<4, KM>(r1 + 16 * tig, kmis, c1);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -404,7 +406,7 @@ __device__ __forceinline__ void p_to_b(const float (&pp)[G == 8 ? 2 : 1][2], int
 // fp16 number: one conversion instruction turns two such bytes into the
 // half2 of an A register.  The accumulators therefore hold 2^-9 of the value
 // sums; the epilogue scales them back by 512 (exact).
-template <int VBITS, int G, bool ALIGNED>
+template <int VBITS, int G, int VM>
 __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, int tig, int vmis,
                                         const uint32_t (&pb)[2][2], float (&acc)[8][4])
 {
@@ -413,15 +415,15 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
     for (int j = 0; j < 4; ++j) {
         const uint8_t* rv = tile_v + (4 * tig + j) * rs;
         if constexpr (VBITS == 4) {
-            lds_words<2, ALIGNED>(rv + 8 * gid, vmis, vw[j]);
+            lds_words<2, VM>(rv + 8 * gid, vmis, vw[j]);
         } else if constexpr (VBITS == 2) {
             uint32_t w[1];
-            lds_words<1, ALIGNED>(rv + 4 * gid, vmis, w);
+            lds_words<1, VM>(rv + 4 * gid, vmis, w);
             vw[j][0] = w[0];
             vw[j][1] = 0u;
         } else {
             uint32_t w[3], n[4];
-            lds_words<3, ALIGNED>(rv + 12 * (gid >> 1), vmis, w);
+            lds_words<3, VM>(rv + 12 * (gid >> 1), vmis, w);
             nibbles3(w, n);
             vw[j][0] = (gid & 1) ? n[2] : n[0];
             vw[j][1] = (gid & 1) ? n[3] : n[1];
@@ -724,9 +726,12 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // One 32-token tile in stage memory st (this warp's slot at offset 0).
     // PARTIAL: some of its tokens lie at or past t_end and are masked.
     // LO: the keys' lo part is needed (all but 2-bit keys with key_alpha)
-    auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag, auto lo_tag) {
+    // KM / VM: the key / value misalignment of this warp's slot (0 or 2)
+    auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag, auto lo_tag,
+                    auto km_tag, auto vm_tag) {
         constexpr bool PARTIAL = decltype(partial_tag)::value;
         constexpr bool LO = decltype(lo_tag)::value;
+        constexpr int KM = decltype(km_tag)::value, VM = decltype(vm_tag)::value;
         // ---- scores of both 16-row tiles
         float s[NH][2][2], vs[2][2], vz[2][2];
         bool ok[2][2];
@@ -737,7 +742,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
-            qk_tile<KMODE, G, LO>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
+            qk_tile<KMODE, G, LO, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
             float n0 = 1.f, n1 = 1.f;
             if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
             vs[rt][0] = lds_f16(m0 + a.g.m_scale);
@@ -836,13 +841,13 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             if (SPARSE && !__any_sync(0xffffffffu, vlive[rt])) continue;   // warp-uniform
             uint32_t pb[2][2];
             p_to_b<G>(pp[rt], gid, tig, pb);
-            pv_tile<VBITS, G, KMODE == 8>(st + 16 * rt * rs + a.g.v_off, rs, gid, tig, vmis, pb, acc);
+            pv_tile<VBITS, G, VM>(st + 16 * rt * rs + a.g.v_off, rs, gid, tig, vmis, pb, acc);
         }
     };
 
     // The tile loop; returns the tile whose wait gave up, or -1.  2-bit keys
     // instantiate it with and without the lo part and pick once per CTA.
-    auto run = [&](auto lo_tag) {
+    auto run = [&](auto lo_tag, auto km_tag, auto vm_tag) {
         int stage = 0;               // it mod NST
         uint32_t parity = 0;         // (it / NST) mod 2
         for (int it = 0; it < ntiles; ++it) {
@@ -853,8 +858,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* st = smem + stage * stage_bytes + hoff;
             const uint8_t* sm = smem + stage * stage_bytes + moff;
             const int t0 = t_begin + it * kTile;
-            if (t0 + kTile <= t_end) tile(st, sm, t0, std::false_type{}, lo_tag);
-            else                     tile(st, sm, t0, std::true_type{}, lo_tag);
+            if (t0 + kTile <= t_end) tile(st, sm, t0, std::false_type{}, lo_tag, km_tag, vm_tag);
+            else                     tile(st, sm, t0, std::true_type{}, lo_tag, km_tag, vm_tag);
 
             // ---- this warp is done with the stage; the last warp refills it
             __syncwarp();
@@ -870,9 +875,24 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
         return -1;
     };
+    // Misalignment of the warp's key and value loads: FP8 keys are read as
+    // aligned words and their values start aligned.  3-bit keys with 3-bit
+    // values run an instantiation per (key, value) misalignment, picked per
+    // warp (4.7% faster on 256K contexts); the other presets test it in the
+    // loop (separate instantiations cost them instruction-cache misses).
+    using M0 = std::integral_constant<int, 0>;
+    using M2 = std::integral_constant<int, 2>;
+    using MR = std::integral_constant<int, -1>;
+    auto run_mis = [&](auto lo_tag) {
+        if constexpr (KMODE == 8) return run(lo_tag, M0{}, M0{});
+        else if constexpr (KMODE == 3 && VBITS == 3) {
+            if (kmis == 0) return vmis == 0 ? run(lo_tag, M0{}, M0{}) : run(lo_tag, M0{}, M2{});
+            else           return vmis == 0 ? run(lo_tag, M2{}, M0{}) : run(lo_tag, M2{}, M2{});
+        } else return run(lo_tag, MR{}, MR{});
+    };
     int failed_at;
-    if constexpr (KMODE == 2) failed_at = key_lo ? run(std::true_type{}) : run(std::false_type{});
-    else                      failed_at = run(std::true_type{});
+    if constexpr (KMODE == 2) failed_at = key_lo ? run_mis(std::true_type{}) : run_mis(std::false_type{});
+    else                      failed_at = run_mis(std::true_type{});
     // stage 2 (a programmatic dependent launch) may start its launch now; it
     // waits for this grid's completion before it reads the partials
     asm volatile("griddepcontrol.launch_dependents;");
