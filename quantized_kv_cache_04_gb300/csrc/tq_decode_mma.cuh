@@ -201,17 +201,12 @@ __device__ __forceinline__ int seq_of_rank(const int32_t* seq_lens, int B, int r
     return b;
 }
 
-// Token of QK row r (0..15) inside a tile.  Rows r and r+8 of a thread hold
-// tokens whose shared-memory rows are 8 apart modulo 8 (fewer bank
-// conflicts), and the four tokens 4m..4m+3 that one PV thread needs come
-// from exactly two QK threads.
-__device__ __forceinline__ int qk_token(int r)
-{
-    const int gid = r & 7, m = gid >> 1, e = gid & 1;
-    const bool second = r >= 8;
-    const bool hi_pair = (m >= 2) != second;   // +2 for (m<2, second row) or (m>=2, first row)
-    return 4 * m + e + (hi_pair ? 2 : 0);
-}
+// Token order inside a 16-row tile: the MMAs' own.  QK row r is token r
+// (thread gid: tokens gid and gid + 8); value k index k is token k (thread
+// tig: tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9, held by the QK threads
+// gid = 2 tig and 2 tig + 1).  With a shared row stride of 4 mod 8 words,
+// the key loads of a warp (8 rows, 12-16 bytes per lane) and its value loads
+// (4 rows 2 tig + c, 8 bytes per lane) touch distinct banks.
 
 __device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two_bytes)
 {
@@ -359,8 +354,8 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
 }
 
 // P' of one 16-row tile to the B layout of the value MMA: thread (gid, tig)
-// feeds column gid for tokens 4 tig .. 4 tig + 3, which QK threads with
-// gid 2 tig and 2 tig + 1 hold (first row = qk_token(gid), second = qk_token(gid + 8)).
+// feeds column gid for tokens 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9
+// (b1), which QK threads with gid 2 tig and 2 tig + 1 hold (rows gid, gid + 8).
 // pp[j][r]: P' of the thread's head j (G = 8: heads 2 tig, 2 tig + 1), row r.
 template <int G>
 __device__ __forceinline__ void p_to_b(const float (&pp)[G == 8 ? 2 : 1][2], int gid, int tig,
@@ -395,12 +390,12 @@ __device__ __forceinline__ void p_to_b(const float (&pp)[G == 8 ? 2 : 1][2], int
         const uint32_t ax = __shfl_sync(0xffffffffu, X, srcA), ay = __shfl_sync(0xffffffffu, Y, srcA);
         const uint32_t bx = __shfl_sync(0xffffffffu, X, srcB), by = __shfl_sync(0xffffffffu, Y, srcB);
         const uint32_t XA = take_y ? ay : ax, XB = take_y ? by : bx;
-        if (tig < 2) { pb[part][0] = prmt(XA, XB, 0x5410u); pb[part][1] = prmt(XA, XB, 0x7632u); }
-        else         { pb[part][0] = prmt(XA, XB, 0x7632u); pb[part][1] = prmt(XA, XB, 0x5410u); }
+        pb[part][0] = prmt(XA, XB, 0x5410u);
+        pb[part][1] = prmt(XA, XB, 0x7632u);
     }
 }
 
-// Value MMAs of one 16-row tile: tokens 4 tig + j of the tile, dims 16 gid + 2i (+1).
+// Value MMAs of one 16-row tile: tokens 2 tig + (j & 1) + 8 (j >> 1), dims 16 gid + 2i (+1).
 // A value code n (0..15) placed alone in a byte and read as FP8 E4M3 is
 // exactly n * 2^-9 (subnormal for n < 8, normal above), and that is a normal
 // fp16 number: one conversion instruction turns two such bytes into the
@@ -410,10 +405,10 @@ template <int VBITS, int G, int VM>
 __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, int tig, int vmis,
                                         const uint32_t (&pb)[2][2], float (&acc)[8][4])
 {
-    uint32_t vw[4][2];   // per token 4 tig + j: nibble words of dims 16 gid .. 16 gid + 15
+    uint32_t vw[4][2];   // per token j of the thread: nibble words of dims 16 gid .. 16 gid + 15
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint8_t* rv = tile_v + (4 * tig + j) * rs;
+        const uint8_t* rv = tile_v + (2 * tig + (j & 1) + 8 * (j >> 1)) * rs;
         if constexpr (VBITS == 4) {
             lds_words<2, VM>(rv + 8 * gid, vmis, vw[j]);
         } else if constexpr (VBITS == 2) {
@@ -431,7 +426,7 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
     }
     // MMAs i and i + 1 (dims 16 gid + 2i .. 2i + 3) share one byte gather:
     // ab = [A_i, B_i, A_i+1, B_i+1] with A, B the tokens of k = 2 tig, 2 tig + 1
-    // (cd likewise for tokens 4 tig + 2, + 3); its low nibbles give row gid
+    // (cd likewise for tokens 2 tig + 8, + 9); its low nibbles give row gid
     // (even dims), its high nibbles row gid + 8 (odd dims).
     if constexpr (VBITS == 2) {
         // byte b of a token's word holds dims 16 gid + 4b .. 4b + 3 (two bits
@@ -714,7 +709,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-    const int tau0 = qk_token(gid), tau1 = qk_token(gid + 8);
+    const int tau0 = gid, tau1 = gid + 8;      // this thread's QK rows
     const int hoff = warp * int(hs_g);         // this warp's slot (SoA: data record) in a shared row
     const int kmis = hoff & 2;
     const int vmis = (hoff + a.g.v_off) & 2;
