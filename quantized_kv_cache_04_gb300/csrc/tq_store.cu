@@ -17,6 +17,8 @@
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
+#include <type_traits>
+
 namespace tq {
 namespace {
 
@@ -33,8 +35,31 @@ struct StoreArgs {
     int num_tokens, num_kv_heads;
     int slot_size;                        // unpadded
     int bs;                               // block_size (SoA record positions)
+    int vec;                              // 1: K and V rows of a head are 8-byte aligned
     SlotGeom g;
 };
+
+// The 4 input elements of lane `lane` for (token n, head h): one 8-byte load
+// when the rows are 8-byte aligned, else four 2-byte loads.
+template <typename T>
+__device__ __forceinline__ uint2 load4(const T* base, long long stride, int n, int h, int lane, bool vec)
+{
+    const T* p = base + n * stride + (long long)h * kHeadDim + 4 * lane;
+    if (vec) return *reinterpret_cast<const uint2*>(p);
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+    return make_uint2(uint32_t(q[0]) | uint32_t(q[1]) << 16, uint32_t(q[2]) | uint32_t(q[3]) << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack4(uint2 r, float (&x)[4])
+{
+    const uint16_t u[4] = {uint16_t(r.x), uint16_t(r.x >> 16), uint16_t(r.y), uint16_t(r.y >> 16)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<T, __half>::value) x[i] = __half2float(__ushort_as_half(u[i]));
+        else x[i] = __bfloat162float(__ushort_as_bfloat16(u[i]));
+    }
+}
 
 // Pack the 4 codes of every lane (code 4*lane+i = c[i]) as a BITS-wide
 // LSB-first bitstream starting at dst (2-byte aligned).  All lanes of the warp
@@ -98,18 +123,31 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
 
     const T* K = static_cast<const T*>(a.key);
     const T* V = static_cast<const T*>(a.value);
+    const bool vec = a.vec != 0;
 
-    for (int n = blockIdx.x; n < a.num_tokens; n += gridDim.x) {
-        const long long slot_idx = a.slot_mapping[n];
+    // The next token's inputs and slot are loaded while this one is encoded.
+    int n = blockIdx.x;
+    uint2 kr = make_uint2(0u, 0u), vr = kr;
+    long long slot_next = -1;
+    if (n < a.num_tokens) {
+        kr = load4(K, a.key_stride, n, h, lane, vec);
+        vr = load4(V, a.value_stride, n, h, lane, vec);
+        slot_next = a.slot_mapping[n];
+    }
+    for (; n < a.num_tokens; n += gridDim.x) {
+        const long long slot_idx = slot_next;
+        float k[4], v[4];
+        unpack4<T>(kr, k);
+        unpack4<T>(vr, v);
+        const int nn = n + gridDim.x;
+        if (nn < a.num_tokens) {
+            kr = load4(K, a.key_stride, nn, h, lane, vec);
+            vr = load4(V, a.value_stride, nn, h, lane, vec);
+            slot_next = a.slot_mapping[nn];
+        }
         if (slot_idx < 0 || slot_idx >= a.num_slots) continue;   // uniform across the CTA
         uint8_t* row = smem;
         uint8_t* dst = row + h * S;
-
-        float k[4], v[4];
-        const T* kp = K + n * a.key_stride + (long long)h * kHeadDim + 4 * lane;
-        const T* vp = V + n * a.value_stride + (long long)h * kHeadDim + 4 * lane;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) { k[i] = to_f32(kp[i]); v[i] = to_f32(vp[i]); }
 
         // ---------------- keys
         if constexpr (KEY_FP8) {
@@ -266,6 +304,10 @@ extern "C" int tq_store(int preset, int head_dim, int num_tokens, int num_kv_hea
     a.slot_size = L.slot_size;
     a.bs = block_size;
     a.g = geom_of(L, is_soa(preset));
+    // 8-byte input loads need 8-byte aligned rows: both bases, and strides of
+    // a multiple of 4 elements
+    a.vec = ((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value)) & 7) == 0 &&
+            key_stride_tok % 4 == 0 && value_stride_tok % 4 == 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = in_dtype == TQ_F16 ? launch_store_t<__half>(preset, a, st)
                                        : launch_store_t<__nv_bfloat16>(preset, a, st);

@@ -99,6 +99,34 @@ def test_store_edge_values(orc, preset):
         _check(orc, preset, K, V, sm, cache, s, c32, m32, bs, bound_fraction=False)
 
 
+@pytest.mark.parametrize("preset", PRESETS)
+def test_store_unaligned_rows(orc, preset):
+    """Input rows that are only 2-byte aligned (a view starting one element
+    into a buffer whose token stride is not a multiple of 4 elements): the
+    store reads them element by element and writes the same slots as for
+    contiguous inputs."""
+    rng = np.random.default_rng(9100 + preset)
+    N, Hk, D, bs = 45, 8, 128, 16
+    K = torch.from_numpy(rng.normal(size=(N, Hk, D))).to(torch.float16)
+    V = torch.from_numpy(rng.normal(size=(N, Hk, D))).to(torch.float16)
+    row = Hk * D + 6
+    kb = torch.zeros((N, row), dtype=torch.float16)
+    vb = torch.zeros((N, row), dtype=torch.float16)
+    kb[:, 1:1 + Hk * D] = K.reshape(N, -1)
+    vb[:, 3:3 + Hk * D] = V.reshape(N, -1)
+    kbd, vbd = kb.cuda(), vb.cuda()
+    kview = kbd[:, 1:1 + Hk * D].view(N, Hk, D)
+    vview = vbd[:, 3:3 + Hk * D].view(N, Hk, D)
+    assert kview.data_ptr() % 8 == 2 and kview.stride(0) % 4 == 2
+    num_blocks = (N + bs - 1) // bs + 1
+    sm = rng.permutation(num_blocks * bs)[:N].astype(np.int64)
+    cache_u, s, c32, m32 = _run_store(orc, preset, K, V, sm, num_blocks, bs,
+                                      key_view=kview, value_view=vview)
+    cache_c, _, _, _ = _run_store(orc, preset, K, V, sm, num_blocks, bs)
+    assert np.array_equal(cache_u, cache_c)
+    _check(orc, preset, K, V, sm, cache_u, s, c32, m32, bs)
+
+
 def test_store_padding_only_and_large_batch(orc):
     """All-padding slot mapping writes nothing; a 16384-token store over 8
     heads matches the oracle on a sample of tokens."""
