@@ -15,10 +15,16 @@
 // The grouped-query tiles are dense after unpacking, so they run as MMAs.
 // Precision: fp16 operands carry 11 bits, so every fp32 quantity that is not
 // exactly representable is split into hi = fp16(x) and lo = fp16(x - hi):
-// q (all presets), the Lloyd-Max centroids of MSE keys, and P' (for G = 4 the
-// spare 4 columns carry the lo parts; for G = 8 a second MMA does).  FP8 keys and integer value codes
-// are exact in fp16.  The value path uses P' = p * v_scale and adds
-// sum_t p_t v_zero_t separately (v_hat = code * scale + zero).
+// q (all presets), the Lloyd-Max centroids of 3- and 4-bit keys, and P' (for
+// G = 4 the spare 4 columns carry the lo parts; for G = 8 a second MMA does).
+// 2-bit centroids are scaled by a factor that makes them fp16-exact (no lo
+// part).  FP8 keys and integer value codes are exact in fp16.  The value
+// path uses P' = p * v_scale and adds sum_t p_t v_zero_t separately
+// (v_hat = code * scale + zero).
+//
+// Launch chain: stage 1 is a programmatic dependent of the previous kernel
+// in the stream and waits for it before its first global read; stage 2 is a
+// programmatic dependent of stage 1.
 //
 // Method sources: "vllm-project/vllm pull 38479" digest, implementation item 4
 // (split-K stage 1 / stage 2); "vllm.v1.attention.backends.turboquant_attn" API
