@@ -370,7 +370,7 @@ def time_dequant(p: "Problem", peak_gbs: float, calls: int = 20):
             "frac_of_measured_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
 
 
-def time_long_context(dev, peak_gbs: float, ctxs=(32768, 262144), presets=tuple(SLOT),
+def time_long_context(dev, peak_gbs: float, ctxs=(32768, 65536, 131072, 262144), presets=tuple(SLOT),
                       calls: int = 50):
     """Decode-only side run at long contexts: the Llama-3-8B shape (bs 16)
     for every preset at each context with batch 2^20 / ctx, the library's
@@ -432,12 +432,33 @@ def _oracle_decode_once(w, smp):
     return time.perf_counter() - t0
 
 
+def _cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm
+    implementer and part numbers)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in info:
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    return " ".join(f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields) or "unknown"
+
+
 def cpu_baseline(w, budget_s: float = 10.0):
     """The oracle's decode on the host, over whole sequences of the workload
-    in order until about budget_s seconds of decode work (or all of them)."""
+    in order until about budget_s seconds of decode work (or all of them):
+    one thread, then the same sequences decoded concurrently by one thread
+    per host core (the oracle's C calls run without the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
     probe = _oracle_sample(w, 256)
     per_tok = _oracle_decode_once(w, probe) / probe["n"]
     nbytes, dec_s, store_s, ntok, nseq = 0, 0.0, 0.0, 0, 0
+    samples = []
     for seq in range(w.B):
         # a sequence longer than the remaining budget contributes a prefix
         n = min(int(w.seq_lens[seq]), max(256, int((budget_s - dec_s) / per_tok)))
@@ -447,10 +468,20 @@ def cpu_baseline(w, budget_s: float = 10.0):
         nbytes += smp["bytes"]
         ntok += smp["n"]
         nseq += 1
+        samples.append(smp)
         if dec_s >= budget_s:
             break
+    ncpu = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=ncpu) as ex:
+        list(ex.map(lambda smp: _oracle_decode_once(w, smp), samples))
+    par_s = time.perf_counter() - t0
     return {"value": round(nbytes / dec_s / 1e9, 6), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": _cpu_model(), "nproc": ncpu,
+            "multi_core": {"value": round(nbytes / par_s / 1e9, 6), "unit": "GB/s",
+                           "cores": min(ncpu, len(samples)),
+                           "sample": f"the same {len(samples)} sequences, one per thread "
+                                     f"({par_s:.1f} s wall)"},
             "sample": (f"sequences 0..{nseq - 1} of {w.B} in order ({ntok} tokens; a sequence "
                        f"past the budget contributes a prefix), all {w.Hk} kv heads, "
                        f"{w.Hq // w.Hk} q heads each: dense fp64 decode over the oracle's cache "
