@@ -341,6 +341,48 @@ def time_store_mixed(dev):
     return res
 
 
+def time_store_large(dev, tokens: int = 1 << 20):
+    """Store throughput at scale: 2^20 tokens (16 sequences of 64K, the
+    Llama-3-8B shape: 8 kv heads, bs 16, bf16) in one call, every preset;
+    median of 10 calls, L2 flushed between them."""
+    import torch
+    import quantized_kv_cache_04_gb300 as tq
+    res = {}
+    for preset in SLOT:
+        w = wl.make("sweep", ctx=tokens // 16, preset=preset)
+        ks, vs, sms = [], [], []
+        for b in range(w.B):
+            n = int(w.seq_lens[b])
+            K, V = wl.gen_kv(w, b, 0, n, dev)
+            ks.append(K)
+            vs.append(V)
+            sms.append(w.slot_mapping(b, np.arange(n)))
+        K, V = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+        del ks, vs
+        sm = torch.from_numpy(np.concatenate(sms)).to(dev)
+        c = tq.TQCache(preset, w.num_blocks, w.block_size, w.Hk, device=dev)
+        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            c.store(K, V, sm)
+        ts = []
+        for _ in range(10):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            c.store(K, V, sm)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = float(np.median(ts))
+        N = K.shape[0]
+        moved = N * w.Hk * (2 * 2 * w.D + SLOT[preset]) + 8 * N
+        res[preset] = {"tokens": N, "ms": round(ms, 4), "mtok_s": round(N / ms / 1e3, 2),
+                       "gbs": round(moved / ms / 1e6, 1)}
+        del K, V, sm, c, flush
+        torch.cuda.empty_cache()
+    return res
+
+
 def time_dequant(p: "Problem", peak_gbs: float, calls: int = 20):
     """Dequantisation side run: every cached token of the workload back to
     fp16 K and V (tq_dequant over the whole slot list).  Bytes = slots read +
@@ -583,6 +625,7 @@ def main():
     if not args.no_extra and rank == 0:
         line["store_mixed"] = time_store_mixed(dev)
         line["store_mtok_s"] = line["store_mixed"]["turboquant_4bit_nc"]["mtok_s"]
+        line["store_1m"] = time_store_large(dev)
         line["dequant"] = time_dequant(p, peak)
         if args.workload == "llama3_8b" and args.ctx is None and args.batch is None:
             line["long_context"] = time_long_context(dev, peak)
