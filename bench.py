@@ -265,29 +265,43 @@ def time_device(p: Problem, steps: int, warmup: int, world: int, gpu_index: int)
 
 def time_e2e(p: Problem, steps: int, warmup: int, world: int):
     """Same step with host inputs: pinned H2D of q, new K/V, slot mapping,
-    block table and seq_lens, then D2H of the attention output and LSE."""
+    block table and seq_lens, then D2H of the attention output and LSE.  The
+    step's inputs sit packed in one pinned buffer and travel in one copy into
+    one device buffer whose views the store and decode take; the output and
+    LSE share one device buffer and come back in one copy."""
     import torch
     st = torch.cuda.current_stream()
-    hq = p.q.cpu().pin_memory()
-    hk, hv = p.new_k.cpu().pin_memory(), p.new_v.cpu().pin_memory()
-    hsm = p.new_sm.cpu().pin_memory()
-    hbt, hsl = p.bt.cpu().pin_memory(), p.sl.cpu().pin_memory()
-    hout = torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory()
-    hlse = torch.empty(p.lse.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hsm, hbt, hsl))
-    d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
+
+    def layout(ts):
+        offs, o = [], 0
+        for t in ts:
+            offs.append(o)
+            o += (t.numel() * t.element_size() + 15) // 16 * 16
+        return offs, o
+
+    def view(buf, off, t):
+        n = t.numel() * t.element_size()
+        return buf[off:off + n].view(t.dtype).view(t.shape)
+
+    ins = [p.q, p.new_k, p.new_v, p.new_sm, p.bt, p.sl]
+    in_offs, in_bytes = layout(ins)
+    hin = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    din = torch.empty(in_bytes, dtype=torch.uint8, device=p.dev)
+    for t, o in zip(ins, in_offs):
+        view(hin, o, t).copy_(t.cpu())
+    p.q, p.new_k, p.new_v, p.new_sm, p.bt, p.sl = [view(din, o, t) for t, o in zip(ins, in_offs)]
+    outs = [p.out, p.lse]
+    out_offs, out_bytes = layout(outs)
+    dout = torch.empty(out_bytes, dtype=torch.uint8, device=p.dev)
+    hout = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    p.out, p.lse = [view(dout, o, t) for t, o in zip(outs, out_offs)]
+    h2d, d2h = in_bytes, out_bytes
 
     def step():
-        p.q.copy_(hq, non_blocking=True)
-        p.new_k.copy_(hk, non_blocking=True)
-        p.new_v.copy_(hv, non_blocking=True)
-        p.new_sm.copy_(hsm, non_blocking=True)
-        p.bt.copy_(hbt, non_blocking=True)
-        p.sl.copy_(hsl, non_blocking=True)
+        din.copy_(hin, non_blocking=True)
         p.store()
         p.decode()
-        hout.copy_(p.out, non_blocking=True)
-        hlse.copy_(p.lse, non_blocking=True)
+        hout.copy_(dout, non_blocking=True)
 
     for _ in range(warmup):
         step()
