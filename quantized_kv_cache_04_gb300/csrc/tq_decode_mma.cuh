@@ -259,11 +259,34 @@ __device__ __forceinline__ void lut16(const uint32_t (&T)[8][2], uint32_t s, uin
     l1 = prmt(x[2], x[3], 0x7362u);
 }
 
+// The same lookup for a symmetric codebook (c_k = -c_(15-k), the Lloyd-Max
+// case): an 8-entry magnitude table per byte plane (T[0] / T[1]: low / high
+// byte of fp16(M_j), T[2] / T[3]: of the fp16 residual, M_j = c_(8+j)) read
+// with j = (code & 7) ^ (bit 3 ? 0 : 7), and the sign of the codes below 8
+// put into the high bytes: PRMT's sign-replicate mode turns each code's bit
+// 3 into a 0x00 / 0xFF byte (bit 3 of codes 0 / 2 is the top bit of bytes
+// 0 / 1 of s << 4, of codes 1 / 3 the top bit of bytes 0 / 1 of s).
+// 15 instructions for four codes against 19.
+__device__ __forceinline__ void lut16_sym(const uint32_t (&T)[8][2], uint32_t s, uint32_t& h0, uint32_t& h1,
+                                          uint32_t& l0, uint32_t& l1)
+{
+    const uint32_t t = (~s >> 3) & 0x1111u;               // 1 where bit 3 is clear
+    const uint32_t j = (s & 0x7777u) ^ (t * 7u);          // magnitude index
+    const uint32_t pos = prmt(s << 4, s, 0xD9C8u);        // 0xFF where bit 3 is set
+    const uint32_t neg = ~pos & 0x80808080u;              // fp16 sign bits of the high bytes
+    const uint32_t p0 = prmt(T[0][0], T[0][1], j), p1 = prmt(T[1][0], T[1][1], j) ^ neg;
+    const uint32_t u0 = prmt(T[2][0], T[2][1], j), u1 = prmt(T[3][0], T[3][1], j) ^ neg;
+    h0 = prmt(p0, p1, 0x5140u);
+    h1 = prmt(p0, p1, 0x7362u);
+    l0 = prmt(u0, u1, 0x5140u);
+    l1 = prmt(u0, u1, 0x7362u);
+}
+
 // Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1: row gid+8).
 // Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
 // MSE keys with G = 8 read their q fragments from shared memory (qsm: this
 // lane's uint4 of k-step 0, stride 32).
-template <int KMODE, int G, bool LO, int KM, int NT>
+template <int KMODE, int G, bool KGEN, int KM, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
                                         const uint4* qsm, const uint32_t (&T)[NT][2], float (&out)[4],
@@ -315,10 +338,13 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
             const uint32_t s0 = c0[kk >> 1] >> (16 * (kk & 1));
             const uint32_t s1 = c1[kk >> 1] >> (16 * (kk & 1));
             uint32_t Ahi[4], Alo[4] = {0u, 0u, 0u, 0u};
-            constexpr bool use_lo = KMODE != 2 || LO;   // 2-bit keys may need no lo part
-            if constexpr (KMODE == 4) {
+            constexpr bool use_lo = KMODE != 2 || KGEN;   // 2-bit keys may need no lo part
+            if constexpr (KMODE == 4 && KGEN) {
                 lut16(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
                 lut16(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
+            } else if constexpr (KMODE == 4) {
+                lut16_sym(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
+                lut16_sym(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
             } else {
                 // 2- and 3-bit keys: one lookup per byte plane, then interleave
                 // the low and high bytes into half2 registers
@@ -688,8 +714,29 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // fp16 residual c - fp16(c), with c = key_alpha * c_k.  2- and 3-bit keys: T[p][k >> 2] holds entries
     // 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
     // plane p of codes 8(k>>3) .. 8(k>>3)+7 in the same way.
+    // 4-bit keys with a symmetric codebook (c_k = -c_(15-k) bit for bit; the
+    // same test in every thread) use the 8-entry magnitude planes instead.
+    bool key_sym = false;
+    if constexpr (KMODE == 4) {
+        key_sym = true;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) key_sym &= a.centroids[k] == -a.centroids[15 - k];
+    }
     uint32_t T[KMODE == 4 ? 8 : 4][2] = {};
-    if constexpr (KMODE != 8) {
+    if (KMODE == 4 && key_sym) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float c = a.centroids[8 + m];
+            const __half chi = __float2half_rn(c);
+            const __half clo = __float2half_rn(c - __half2float(chi));
+            const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
+            const int sh = 8 * (m & 3), w = m >> 2;
+            T[0][w] |= (hb & 0xFFu) << sh;
+            T[1][w] |= (hb >> 8) << sh;
+            T[2][w] |= (lb & 0xFFu) << sh;
+            T[3][w] |= (lb >> 8) << sh;
+        }
+    } else if constexpr (KMODE != 8) {
         constexpr int NC = 1 << KMODE;
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
@@ -726,12 +773,13 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 
     // One 32-token tile in stage memory st (this warp's slot at offset 0).
     // PARTIAL: some of its tokens lie at or past t_end and are masked.
-    // LO: the keys' lo part is needed (all but 2-bit keys with key_alpha)
+    // KGEN: the general key path; false: 2-bit keys without the lo part
+    // (key_alpha), 4-bit keys read through the symmetric lookup (key_sym)
     // KM / VM: the key / value misalignment of this warp's slot (0 or 2)
     auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag, auto lo_tag,
                     auto km_tag, auto vm_tag) {
         constexpr bool PARTIAL = decltype(partial_tag)::value;
-        constexpr bool LO = decltype(lo_tag)::value;
+        constexpr bool KGEN = decltype(lo_tag)::value;
         constexpr int KM = decltype(km_tag)::value, VM = decltype(vm_tag)::value;
         // ---- scores of both 16-row tiles
         float s[NH][2][2], vs[2][2], vz[2][2];
@@ -743,7 +791,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
-            qk_tile<KMODE, G, LO, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
+            qk_tile<KMODE, G, KGEN, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
             float n0 = 1.f, n1 = 1.f;
             if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
             vs[rt][0] = lds_f16(m0 + a.g.m_scale);
@@ -893,6 +941,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     };
     int failed_at;
     if constexpr (KMODE == 2) failed_at = key_lo ? run_mis(std::true_type{}) : run_mis(std::false_type{});
+    else if constexpr (KMODE == 4) failed_at = key_sym ? run_mis(std::false_type{}) : run_mis(std::true_type{});
     else                      failed_at = run_mis(std::true_type{});
     // stage 2 (a programmatic dependent launch) may start its launch now; it
     // waits for this grid's completion before it reads the partials

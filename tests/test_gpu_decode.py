@@ -111,6 +111,23 @@ def test_decode_custom_codebook(orc, preset, G, Hk, bs, seq_lens):
     check_decode(o, l, ref_o, ref_l, f"preset {preset} custom codebook")
 
 
+@pytest.mark.parametrize("preset", [0, 2])
+@pytest.mark.parametrize("B", [512, 520])
+def test_decode_large_varlen_batch(orc, preset, B):
+    """Many short sequences of mixed lengths (0..70 tokens): CTA rows take
+    the sequences longest first up to 512 sequences and in index order
+    beyond; both give the oracle's result."""
+    rng = np.random.default_rng(9700 + B + preset)
+    Hk, G, bs = 8, 4, 16
+    seq_lens = rng.integers(0, 71, size=B)
+    pb = paged_problem(orc, preset, seq_lens, Hk, bs, rng)
+    q = torch.from_numpy(rng.normal(size=(B, G * Hk, 128))).to(torch.float16)
+    ref_o, ref_l = orc.decode_dense(preset, to_f32(q), pb["cache"], pb["bt"],
+                                    np.asarray(seq_lens, np.int32), Hk, bs, pb["signs"], pb["c32"])
+    o, l = _gpu_decode(preset, q, pb["cache"], pb["bt"], seq_lens, Hk, bs, pb["signs"], pb["c32"], 3)
+    check_decode(o, l, ref_o, ref_l, f"preset {preset} B {B}")
+
+
 @pytest.mark.parametrize("preset", PRESETS)
 def test_split_count_invariance(orc, preset):
     """Results do not depend on the split count beyond rounding."""
