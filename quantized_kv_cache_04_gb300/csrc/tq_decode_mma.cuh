@@ -214,13 +214,6 @@ __device__ __forceinline__ int seq_of_rank(const int32_t* seq_lens, int B, int r
 // the key loads of a warp (8 rows, 12-16 bytes per lane) and its value loads
 // (4 rows 2 tig + c, 8 bytes per lane) touch distinct banks.
 
-__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two_bytes)
-{
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu),
-                                                     __NV_E4M3);
-    return uint32_t(h.x) | (uint32_t(h.y) << 16);
-}
-
 __device__ __forceinline__ float fast_exp2(float x)
 {
     float y;
