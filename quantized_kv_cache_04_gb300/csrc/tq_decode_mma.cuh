@@ -574,28 +574,40 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         uint8_t* dst = smem + stage * stage_bytes;
         uint64_t* bar = &full[stage];
         const int tbase = t_begin + tile * kTile;
-        const bool per_segment = rs == drow && cb == drow && (!soa || mb == a.Hk * a.g.meta_bytes);
-        const int nseg = per_segment ? kTile / seg_rows : kTile;     // copies per tile and region
-        const int seg_len = per_segment ? seg_rows : 1;               // rows per copy
-        const int nlive = min(nseg, (L - tbase + seg_len - 1) / seg_len);
+        // data rows: one copy per page segment when the CTA takes whole rows
+        // and the shared stride equals the global one, else one per row;
+        // SoA metadata rows (unpadded in shared memory): one copy per page
+        // segment when the CTA takes every kv head
+        const bool seg_d = rs == drow && cb == drow;
+        const bool seg_m = soa && mb == a.Hk * a.g.meta_bytes;
+        const int len_d = seg_d ? seg_rows : 1, len_m = seg_m ? seg_rows : 1;   // rows per copy
+        const int nd = min(kTile / len_d, (L - tbase + len_d - 1) / len_d);
+        const int nm = soa ? min(kTile / len_m, (L - tbase + len_m - 1) / len_m) : 0;
         if (lane == 0) {
             fence_async_shared();             // prior generic reads of this stage before the async writes
-            mbar_expect_tx(bar, uint32_t(nlive * seg_len * (cb + mb)));
+            mbar_expect_tx(bar, uint32_t(nd * len_d * cb + nm * len_m * mb));
         }
         __syncwarp();
-        if (lane < nlive) {
-            const int t = tbase + lane * seg_len;
+        const bool same = !soa || len_d == len_m;     // one address computation for both copies
+        if (lane < nd) {
+            const int t = tbase + lane * len_d;
             const long long page = bt[t >> lg];
             const int off = t & ((1 << lg) - 1);
-            if (soa) {
-                const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
-                bulk_g2s(dst + lane * seg_len * rs, blk + off * drow + h0 * hs_g, uint32_t(seg_len * cb), bar);
+            const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
+            const uint8_t* src = soa ? blk + off * drow + h0 * hs_g : blk + off * (long long)row_bytes + h0 * hs_g;
+            bulk_g2s(dst + lane * len_d * rs, src, uint32_t(len_d * cb), bar);
+            if (soa && same) {
                 const uint8_t* meta = blk + (1LL << lg) * drow + ((long long)off * a.Hk + h0) * a.g.meta_bytes;
-                bulk_g2s(dst + kTile * rs + lane * seg_len * mb, meta, uint32_t(seg_len * mb), bar);
-            } else {
-                const uint8_t* src = a.cache + ((page << lg) + off) * (long long)row_bytes + h0 * hs_g;
-                bulk_g2s(dst + lane * seg_len * rs, src, uint32_t(seg_len * cb), bar);
+                bulk_g2s(dst + kTile * rs + lane * len_m * mb, meta, uint32_t(len_m * mb), bar);
             }
+        }
+        if (!same && lane < nm) {
+            const int t = tbase + lane * len_m;
+            const long long page = bt[t >> lg];
+            const int off = t & ((1 << lg) - 1);
+            const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
+            const uint8_t* meta = blk + (1LL << lg) * drow + ((long long)off * a.Hk + h0) * a.g.meta_bytes;
+            bulk_g2s(dst + kTile * rs + lane * len_m * mb, meta, uint32_t(len_m * mb), bar);
         }
     };
     // The q staging area (hpc x (4 or 8) heads x 512 B) sits at the end of the
