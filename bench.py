@@ -221,13 +221,21 @@ def _barrier(world):
 
 
 def _max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values (the slowest replica's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_value(kv_bytes_per_rank: int, step_ms: float, world: int) -> float:
+    """Whole-job GB/s: every replica reads its own cache each step, and the
+    step time is the slowest replica's."""
+    return world * kv_bytes_per_rank / (step_ms * 1e-3) / 1e9
 
 
 def time_device(p: Problem, steps: int, warmup: int, world: int, gpu_index: int):
@@ -599,7 +607,7 @@ def main():
     step_ms = _max_over_ranks(total_ms / args.steps, world)
     dec_ms = _max_over_ranks(dec_ms, world)
     kvb = _kv_bytes(w)
-    value = world * kvb / (step_ms * 1e-3) / 1e9
+    value = _job_value(kvb, step_ms, world)
 
     e2e_steps = args.e2e_steps or max(10, min(args.steps, 500))
     e2e_ms, h2d, d2h = time_e2e(p, e2e_steps, 3, world)
