@@ -220,7 +220,13 @@ size_t tq_decode_workspace_bytes(int batch, int num_q_heads, int num_splits, int
  * seq_lens[b] == 0 gives o = 0 and lse = -inf.
  * query: device (B, Hq, D) contiguous, q_dtype F16/BF16.
  * kv_cache: device, layout above.  block_table: device int32; entries
- *   at or past ceil(seq_lens[b]/block_size) are never read.
+ *   at or past ceil(seq_lens[b]/block_size) are never read.  An entry that is
+ *   read and lies outside [0, num_blocks) is a caller error: both stage-1
+ *   kernels check each page before reading it, read nothing outside the
+ *   cache, and the query heads of that sequence come out NaN (output and
+ *   lse); other sequences are unaffected (num_blocks = 0: every sequence
+ *   with tokens).  The table must hold
+ *   ceil(seq_lens[b]/block_size) entries per row (not checked).
  * seq_lens: device int32[B].  max_seq_len: host upper bound of seq_lens.
  * softmax_scale: usually 1/sqrt(head_dim).  num_splits: 0 = tq_decode_pick_splits.
  * signs / centroids: device, as for tq_store (centroids may be NULL for k8v4).

@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
         }
         return;
     }
+    __shared__ int s_bad;        // a block-table entry outside [0, num_blocks) was met
+    if (threadIdx.x == 0) s_bad = 0;
     if constexpr (!KEY_FP8) {
         if (threadIdx.x < (1 << KBITS)) s_cent[threadIdx.x] = a.centroids[threadIdx.x];
     }
@@ -142,8 +144,10 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
     }
 
     const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
+    bool bad = false;
     for (int t = t0 + warp; t < t1; t += kWarps) {
         const long long page = bt[t / a.bs];
+        if (page < 0 || page >= a.num_blocks) { bad = true; continue; }   // not read; the rows become NaN
         const uint8_t *sp, *mp;              // data and metadata of the record
         slot_ptrs(a.g, a.cache, page, t % a.bs, h, a.bs, a.Hk, sp, mp);
 
@@ -198,6 +202,7 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
     }
 
     // merge the four warps' partials
+    if (bad && lane == 0) s_bad = 1;
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
         if (lane == 0) { s_m[warp][g] = m[g]; s_l[warp][g] = l[g]; }
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
         }
         float* mp = a.mid + (((long long)b * a.Hq + h * G + g) * S + split) * (kHeadDim + 1);
         mp[d] = o / lsum;
-        if (d == 0) mp[kHeadDim] = M + logf(lsum);
+        if (d == 0) mp[kHeadDim] = s_bad ? __int_as_float(0x7fc00000) : M + logf(lsum);
     }
 }
 
@@ -229,7 +234,7 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
 // arithmetic; lane l owns dims 4l..4l+3.  The R partial merges (running max
 // M, weight sum W, weighted output) are combined through shared memory by
 // the row's first warp.  A NaN lse (a split that gave up waiting for its
-// data) makes the row NaN.
+// data, or met a block-table entry outside the cache) makes the row NaN.
 constexpr int kStage2Warps = 8;
 
 template <typename TO>
@@ -511,7 +516,7 @@ extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (mma_stage1_supported(L, soa, num_kv_heads, a.G)) {
-        rc = launch_mma_stage1(L, soa, q_dtype, query, kv_cache, block_table, block_table_stride, seq_lens,
+        rc = launch_mma_stage1(L, soa, q_dtype, query, kv_cache, num_blocks, block_table, block_table_stride, seq_lens,
                                softmax_scale, S, signs, centroids, a.mid, batch, num_q_heads,
                                num_kv_heads, block_size, v_threshold, st);
         if (rc) return rc;

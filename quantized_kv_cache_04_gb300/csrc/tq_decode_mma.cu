@@ -155,7 +155,7 @@ void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group,
 }
 
 int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* query, const uint8_t* kv_cache,
-                      const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                      long long num_blocks, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
                       float v_threshold, cudaStream_t st)
@@ -165,6 +165,7 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
     a.key_alpha = (!L.key_fp8 && L.key_bits == 2) ? two_bit_alpha() : 0.f;
     a.query = query;
     a.cache = kv_cache;
+    a.num_blocks = num_blocks;
     a.block_table = block_table;
     a.bt_stride = bt_stride;
     a.seq_lens = seq_lens;

@@ -42,6 +42,7 @@ namespace tq {
 struct MmaArgs {
     const void* query;
     const uint8_t* cache;
+    long long num_blocks;    // block-table entries outside [0, num_blocks) are caller errors
     const int32_t* block_table;
     int bt_stride;
     const int32_t* seq_lens;
@@ -526,11 +527,14 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     const int t_begin = split * chunk;
     const int t_end = min(L, t_begin + chunk);
 
-    if (t_begin >= t_end) {      // empty split: lse = -inf and a zero partial
+    if (t_begin >= t_end || a.num_blocks <= 0) {
+        // empty split: lse = -inf and a zero partial; tokens but no cache
+        // block to read them from: a NaN lse
+        const float lse0 = t_begin >= t_end ? -INFINITY : __int_as_float(0x7fc00000);
         for (int i = threadIdx.x; i < Hc * Greal * (kHeadDim + 1); i += blockDim.x) {
             const int hq = h0 * Greal + i / (kHeadDim + 1), d = i % (kHeadDim + 1);
             float* m = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
-            m[d] = d == kHeadDim ? -INFINITY : 0.f;
+            m[d] = d == kHeadDim ? lse0 : 0.f;
         }
         return;
     }
@@ -555,8 +559,12 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // refills it, so warps never wait on each other, only on data.
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * stage_bytes);
     int* done = reinterpret_cast<int*>(full + NST);
+    int* bad_pages = done + NST;               // a block-table entry outside the cache was met
+    int* finished = bad_pages + 1;             // warps past their epilogue
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); done[i] = 0; }
+        *bad_pages = 0;
+        *finished = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -569,6 +577,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     constexpr bool soa = SOA;                  // the block convention (a.g.soa), fixed per instantiation
     const long long hs_g = soa ? a.g.data_bytes : a.g.slot;    // head stride in a global data row
     const long long drow = soa ? (long long)a.Hk * a.g.data_bytes : row_bytes;
+    bool bad_seen = false;                     // this lane replaced a page outside the cache
     auto issue = [&](int tile, int stage) {   // called by all lanes of one warp
         if (tile >= ntiles) return;
         uint8_t* dst = smem + stage * stage_bytes;
@@ -589,9 +598,13 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
         __syncwarp();
         const bool same = !soa || len_d == len_m;     // one address computation for both copies
+        // a block-table entry outside [0, num_blocks) is replaced by page 0,
+        // so nothing outside the cache is read, and noted: the CTA's rows
+        // come out NaN (see the end of the kernel)
         if (lane < nd) {
             const int t = tbase + lane * len_d;
-            const long long page = bt[t >> lg];
+            long long page = bt[t >> lg];
+            if ((unsigned long long)page >= (unsigned long long)a.num_blocks) { page = 0; bad_seen = true; }
             const int off = t & ((1 << lg) - 1);
             const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
             const uint8_t* src = soa ? blk + off * drow + h0 * hs_g : blk + off * (long long)row_bytes + h0 * hs_g;
@@ -603,7 +616,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
         if (!same && lane < nm) {
             const int t = tbase + lane * len_m;
-            const long long page = bt[t >> lg];
+            long long page = bt[t >> lg];
+            if ((unsigned long long)page >= (unsigned long long)a.num_blocks) { page = 0; bad_seen = true; }
             const int off = t & ((1 << lg) - 1);
             const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
             const uint8_t* meta = blk + (1LL << lg) * drow + ((long long)off * a.Hk + h0) * a.g.meta_bytes;
@@ -951,6 +965,26 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // stage 2 (a programmatic dependent launch) may start its launch now; it
     // waits for this grid's completion before it reads the partials
     asm volatile("griddepcontrol.launch_dependents;");
+    // Run by every warp once its partials are written.  If any warp's copies
+    // replaced a page outside the cache, the last warp to get here (when
+    // every epilogue of the CTA is done) gives all the CTA's heads a NaN lse.
+    auto finish = [&]() {
+        __syncwarp();                          // the warp's partial writes before lane 0's count
+        const bool wbad = __any_sync(0xffffffffu, bad_seen);
+        int last = 0;
+        if (lane == 0) {
+            if (wbad) atomicOr(bad_pages, 1);
+            __threadfence_block();
+            last = atomicAdd(finished, 1) == nwarps - 1;
+            __threadfence_block();
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
+        if (last && *reinterpret_cast<volatile int*>(bad_pages))
+            for (int i = lane; i < Hc * Greal; i += 32)
+                a.mid[(((long long)b * Hq + h0 * Greal + i) * S + split) * (kHeadDim + 1) + kHeadDim] =
+                    __int_as_float(0x7fc00000);
+    };
     if (failed_at >= 0) {
         // let the copies that may still be in flight (tiles failed_at ..
         // failed_at + NST - 1) land, with the same bounded wait, then mark
@@ -960,6 +994,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         if (lane < Greal)
             a.mid[(((long long)b * Hq + h * Greal + lane) * S + split) * (kHeadDim + 1) + kHeadDim] =
                 __int_as_float(0x7fc00000);
+        finish();
         return;
     }
 
@@ -991,6 +1026,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
         if (gid == 0) mp[kHeadDim] = (m_run[j] + log2f(l_run[j])) * 0.6931471805599453f;
     }
+    finish();
 }
 
 template <typename TQ, int KMODE, int VBITS, int G, bool SPARSE>

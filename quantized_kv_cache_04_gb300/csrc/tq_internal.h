@@ -97,7 +97,7 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
 void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int num_sms,
                       int* ctas_per_split, int* slots);
 int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* query, const uint8_t* kv_cache,
-                      const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                      long long num_blocks, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
                       float v_threshold, cudaStream_t st);

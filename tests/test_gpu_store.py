@@ -171,3 +171,36 @@ def test_store_soa_is_the_aos_rearranged(orc, preset, Hk, bs):
     assert np.array_equal(soa[touched], aos_to_soa(orc, preset, aos[touched]))
     rest = np.setdiff1d(np.arange(nb), touched)
     assert np.all(soa[rest] == SENTINEL)
+
+
+@pytest.mark.parametrize("preset", PRESETS)
+def test_store_skips_slots_outside_the_cache(orc, preset):
+    """Slots at or past num_blocks * block_size (and negative ones) are not
+    written.  The cache handed to the store is a view of the first num_blocks
+    blocks of a larger buffer, so the slots past it still name memory this
+    process owns: the two blocks after the view must keep the sentinel."""
+    rng = np.random.default_rng(9800 + preset)
+    N, Hk, bs, num_blocks = 96, 4, 16, 4
+    L = tq.tq_get_layout(preset)
+    dev = torch.device("cuda")
+    K = torch.from_numpy(rng.normal(size=(N, Hk, 128))).to(torch.float16)
+    V = torch.from_numpy(rng.normal(size=(N, Hk, 128))).to(torch.float16)
+    nslots = num_blocks * bs
+    sm = np.concatenate([rng.permutation(nslots)[:N - 32],
+                         nslots + rng.permutation(2 * bs)[:24], [-1] * 8]).astype(np.int64)
+    rng.shuffle(sm)
+    big = torch.full((num_blocks + 2, bs, Hk, L["slot_size_aligned"]), SENTINEL, dtype=torch.uint8,
+                     device=dev)
+    cache = big[:num_blocks]
+    s = orc.signs(128, 42)
+    c32, m32 = codebook(orc, preset)
+    cc = torch.from_numpy(c32).to(dev) if not L["key_fp8"] else None
+    mm = torch.from_numpy(m32).to(dev) if not L["key_fp8"] else None
+    tq.store(preset, K.to(dev), V.to(dev), torch.from_numpy(sm).to(dev), cache, bs,
+             torch.from_numpy(s).to(dev), cc, mm)
+    torch.cuda.synchronize()
+    out = big.cpu().numpy()
+    assert np.all(out[num_blocks:] == SENTINEL)
+    live = (sm >= 0) & (sm < nslots)
+    lt = torch.from_numpy(live)
+    _check(orc, preset, K[lt], V[lt], sm[live], out[:num_blocks], s, c32, m32, bs)
