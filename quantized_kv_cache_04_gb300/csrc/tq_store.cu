@@ -9,14 +9,17 @@
 // Mapping: one CTA per token (grid-stride), one warp per kv head, 4 consecutive
 // coordinates per lane.  The rotation is a warp-shuffle Walsh-Hadamard
 // transform in registers; the bucketize is a branch-free binary search over
-// midpoints in shared memory; each warp assembles its slot in shared memory
-// and the CTA writes the token's Hk contiguous slots with 16-byte stores.
+// midpoints in shared memory; each warp writes its slot straight into the
+// cache (the SoA convention stages the token's slots in shared memory and
+// scatters their data and metadata records).  Warps of a CTA do not wait
+// for each other in the AoS form.
 // The value path uses explicitly rounded fp32 operations so the stored bytes
 // are reproducible bit for bit.
 #include "tq.h"
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
+#include <atomic>
 #include <type_traits>
 
 namespace tq {
@@ -125,29 +128,42 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
     const T* V = static_cast<const T*>(a.value);
     const bool vec = a.vec != 0;
 
-    // The next token's inputs and slot are loaded while this one is encoded.
+    // The inputs and slots of the next two tokens are in flight while this
+    // one is encoded.
     int n = blockIdx.x;
-    uint2 kr = make_uint2(0u, 0u), vr = kr;
-    long long slot_next = -1;
-    if (n < a.num_tokens) {
-        kr = load4(K, a.key_stride, n, h, lane, vec);
-        vr = load4(V, a.value_stride, n, h, lane, vec);
-        slot_next = a.slot_mapping[n];
+    uint2 kr[2], vr[2];
+    long long sl[2] = {-1, -1};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int m = n + u * gridDim.x;
+        kr[u] = vr[u] = make_uint2(0u, 0u);
+        if (m < a.num_tokens) {
+            kr[u] = load4(K, a.key_stride, m, h, lane, vec);
+            vr[u] = load4(V, a.value_stride, m, h, lane, vec);
+            sl[u] = a.slot_mapping[m];
+        }
     }
     for (; n < a.num_tokens; n += gridDim.x) {
-        const long long slot_idx = slot_next;
+        const long long slot_idx = sl[0];
         float k[4], v[4];
-        unpack4<T>(kr, k);
-        unpack4<T>(vr, v);
-        const int nn = n + gridDim.x;
+        unpack4<T>(kr[0], k);
+        unpack4<T>(vr[0], v);
+        kr[0] = kr[1];
+        vr[0] = vr[1];
+        sl[0] = sl[1];
+        const int nn = n + 2 * gridDim.x;
         if (nn < a.num_tokens) {
-            kr = load4(K, a.key_stride, nn, h, lane, vec);
-            vr = load4(V, a.value_stride, nn, h, lane, vec);
-            slot_next = a.slot_mapping[nn];
+            kr[1] = load4(K, a.key_stride, nn, h, lane, vec);
+            vr[1] = load4(V, a.value_stride, nn, h, lane, vec);
+            sl[1] = a.slot_mapping[nn];
         }
         if (slot_idx < 0 || slot_idx >= a.num_slots) continue;   // uniform across the CTA
+        // AoS: each warp writes its slot straight to the cache (the token's
+        // Hk slots are one contiguous row); SoA: slots are staged in shared
+        // memory and scattered by the CTA
+        const bool soa = a.g.soa;
         uint8_t* row = smem;
-        uint8_t* dst = row + h * S;
+        uint8_t* dst = soa ? row + h * S : a.cache + slot_idx * (long long)row_bytes + h * S;
 
         // ---------------- keys
         if constexpr (KEY_FP8) {
@@ -193,11 +209,22 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
             const __half scale16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), float(QMAX)));
             const __half zero16 = __float2half_rn(lo);
             const float sc = __half2float(scale16), z = __half2float(zero16);
+            // code = rint((v - z) / sc) with the division correctly rounded.
+            // t * fl(1/sc) is within 2^-18 of that quotient (both below 16,
+            // two roundings of 2^-24 relative); it takes the same rint unless
+            // it lies within 2^-16 of a half-integer, where the exact
+            // division decides.
+            const float rsc = sc > 0.f ? __frcp_rn(sc) : 0.f;
             int code[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float r = 0.f;
-                if (sc > 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[i], z), sc)), 0.f), float(QMAX));
+                if (sc > 0.f) {
+                    const float t = __fsub_rn(v[i], z);
+                    float q = __fmul_rn(t, rsc);
+                    if (fabsf(q - (floorf(q) + 0.5f)) < 0x1p-16f) q = __fdiv_rn(t, sc);
+                    r = fminf(fmaxf(rintf(q), 0.f), float(QMAX));
+                }
                 code[i] = int(r);
             }
             pack_codes<VBITS>(dst + a.g.off_v_data, code, lane);
@@ -207,12 +234,12 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
                 if (a.slot_size < S) dst[S - 1] = 0;
             }
         }
+        if (!soa) continue;
         __syncthreads();
 
-        // ---------------- write the token's Hk contiguous slots (AoS), or its
-        // Hk data records and Hk metadata records (SoA), from the staged slots
-        uint8_t* out = a.cache + slot_idx * (long long)row_bytes;
-        if (a.g.soa) {
+        // ---------------- SoA: the token's Hk data records and Hk metadata
+        // records from the staged slots
+        {
             const int Hk = a.num_kv_heads, kd = a.g.key_data_bytes;
             const long long page = slot_idx / a.bs;
             const int off = int(slot_idx - page * a.bs);
@@ -232,34 +259,55 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
                                            : (f == 0 ? a.g.off_k_norm : f == 1 ? a.g.off_v_scale : a.g.off_v_zero);
                 md[i] = *reinterpret_cast<const uint16_t*>(row + hh * S + fo);
             }
-        } else if ((row_bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-            const uint4* src4 = reinterpret_cast<const uint4*>(row);
-            uint4* dst4 = reinterpret_cast<uint4*>(out);
-            for (int i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) dst4[i] = src4[i];
-        } else {
-            const uint16_t* src2 = reinterpret_cast<const uint16_t*>(row);
-            uint16_t* dst2 = reinterpret_cast<uint16_t*>(out);
-            for (int i = threadIdx.x; i < row_bytes / 2; i += blockDim.x) dst2[i] = src2[i];
         }
         __syncthreads();
     }
 }
 
-template <typename T>
-cudaError_t launch_store_t(int preset, const StoreArgs& a, cudaStream_t st)
+// Grid of the grid-stride store: every CTA takes the same number of tokens,
+// so the grid is the CTAs that fit on the device at once (one wave; a second
+// partial wave would finish last with a whole share each).  Resident CTAs
+// per SM are asked once per (device, kv heads) and kept.
+template <typename Kern>
+int store_grid(Kern kernel, int num_kv_heads, size_t smem, int num_tokens)
+{
+    static std::atomic<int> cache[16][33];     // devices x kv heads: resident CTAs on the device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); dev = 0; }
+    int n = (dev >= 0 && dev < 16) ? cache[dev][num_kv_heads].load(std::memory_order_relaxed) : 0;
+    if (n <= 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = kNumSMs;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * num_kv_heads, smem) != cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 4;
+        cudaGetLastError();
+        n = sms * per_sm;
+        if (dev >= 0 && dev < 16) cache[dev][num_kv_heads].store(n, std::memory_order_relaxed);
+    }
+    return num_tokens < n ? num_tokens : n;
+}
+
+template <typename Kern>
+cudaError_t launch_one(Kern kernel, const StoreArgs& a, cudaStream_t st)
 {
     const int threads = 32 * a.num_kv_heads;
     const size_t smem = size_t(a.num_kv_heads) * a.g.slot;
-    int grid = a.num_tokens < kNumSMs * 8 ? a.num_tokens : kNumSMs * 8;
+    kernel<<<store_grid(kernel, a.num_kv_heads, smem, a.num_tokens), threads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_store_t(int preset, const StoreArgs& a, cudaStream_t st)
+{
     switch (preset & 0xFF) {
-    case TQ_K8V4:    store_kernel<T, true, 4, 4, false><<<grid, threads, smem, st>>>(a); break;
-    case TQ_4BIT_NC: store_kernel<T, false, 4, 4, true><<<grid, threads, smem, st>>>(a); break;
-    case TQ_K3V4_NC: store_kernel<T, false, 3, 4, true><<<grid, threads, smem, st>>>(a); break;
-    case TQ_3BIT_NC: store_kernel<T, false, 3, 3, true><<<grid, threads, smem, st>>>(a); break;
-    case TQ_2BIT_NC: store_kernel<T, false, 2, 2, true><<<grid, threads, smem, st>>>(a); break;
+    case TQ_K8V4:    return launch_one(store_kernel<T, true, 4, 4, false>, a, st);
+    case TQ_4BIT_NC: return launch_one(store_kernel<T, false, 4, 4, true>, a, st);
+    case TQ_K3V4_NC: return launch_one(store_kernel<T, false, 3, 4, true>, a, st);
+    case TQ_3BIT_NC: return launch_one(store_kernel<T, false, 3, 3, true>, a, st);
+    case TQ_2BIT_NC: return launch_one(store_kernel<T, false, 2, 2, true>, a, st);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
