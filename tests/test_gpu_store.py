@@ -100,6 +100,32 @@ def test_store_edge_values(orc, preset):
 
 
 @pytest.mark.parametrize("preset", PRESETS)
+def test_store_value_code_ties(orc, preset):
+    """Value rows whose quotients (v - zero) / scale are exact half-integers
+    (scale 1 and 0.25, exact in fp16) or lie within fp16 rounding of one
+    (scale 0.3): the codes must round half to even exactly as the oracle's
+    correctly rounded fp32 division does, bit for bit."""
+    L = tq.tq_get_layout(preset)
+    qmax = 2 ** L["value_bits"] - 1
+    rng = np.random.default_rng(9900 + preset)
+    Hk, D, bs = 2, 128, 16
+    rows = []
+    for lo, step in ((0.0, 1.0), (-3.0, 0.25), (0.0, 0.3), (7.0, 0.3)):
+        half = lo + (np.arange(D) % qmax + 0.5) * step
+        half[0], half[1] = lo, lo + qmax * step          # fix the min and the max
+        rows.append(half)
+    rows.append(rng.permutation(rows[1]))
+    N = len(rows)
+    V = torch.from_numpy(np.stack([np.stack([r] * Hk) for r in rows])).to(torch.float16)
+    for dtype in (torch.float16, torch.bfloat16):
+        Vd = V.to(dtype)
+        K = torch.from_numpy(rng.normal(size=(N, Hk, D))).to(dtype)
+        sm = np.arange(N, dtype=np.int64) * 2
+        cache, s, c32, m32 = _run_store(orc, preset, K, Vd, sm, (2 * N) // bs + 2, bs)
+        _check(orc, preset, K, Vd, sm, cache, s, c32, m32, bs, bound_fraction=False)
+
+
+@pytest.mark.parametrize("preset", PRESETS)
 def test_store_unaligned_rows(orc, preset):
     """Input rows that are only 2-byte aligned (a view starting one element
     into a buffer whose token stride is not a multiple of 4 elements): the
