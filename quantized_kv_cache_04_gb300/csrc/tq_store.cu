@@ -210,10 +210,11 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
             const __half zero16 = __float2half_rn(lo);
             const float sc = __half2float(scale16), z = __half2float(zero16);
             // code = rint((v - z) / sc) with the division correctly rounded.
-            // t * fl(1/sc) is within 2^-18 of that quotient (both below 16,
-            // two roundings of 2^-24 relative); it takes the same rint unless
-            // it lies within 2^-16 of a half-integer, where the exact
-            // division decides.
+            // For quotients below 16, t * fl(1/sc) is within 2^-19 of the
+            // correctly rounded one (three roundings of at most 2^-24
+            // relative), so both take the same rint unless t * fl(1/sc) lies
+            // within 2^-16 of a half-integer, where the exact division
+            // decides; larger quotients clamp to QMAX either way.
             const float rsc = sc > 0.f ? __frcp_rn(sc) : 0.f;
             int code[4];
 #pragma unroll
