@@ -90,7 +90,7 @@ typedef enum { TQ_F16 = 0, TQ_BF16 = 1, TQ_F32 = 2 } tq_dtype;
 typedef struct {
     int key_fp8;            /* 1: keys are FP8 E4M3, unrotated, no norm      */
     int key_bits;           /* 8 (fp8) or Lloyd-Max code width 2/3/4          */
-    int value_bits;         /* uniform value code width 3/4                   */
+    int value_bits;         /* uniform value code width 2/3/4                 */
     int norm_correction;    /* 1: stored norm is ||k|| / ||c[idx]||           */
     int n_centroids;        /* 2^key_bits for MSE keys, 0 for fp8             */
     int key_data_bytes;     /* D (fp8) or ceil(D*key_bits/8)                  */
@@ -139,7 +139,9 @@ int tq_make_signs(int head_dim, uint64_t seed, int8_t* signs);
  *     k_norm = fp16(n_k / ||c[idx]||) (norm correction) or fp16(n_k).
  *   FP8 keys: E4M3 of each coordinate, round to nearest even, saturating.
  *   Values: scale = fp16((max-min)/(2^b_v-1)), zero = fp16(min),
- *     code = clamp(rint((v - zero)/scale), 0, 2^b_v-1), 0 when scale == 0.
+ *     code = clamp(rint((v - zero)/scale), 0, 2^b_v-1), 0 when scale == 0, with
+ *     v - zero and the quotient each correctly rounded in fp32 and rint
+ *     rounding half to even.
  * key, value: device, element type in_dtype, element (n, h, d) at
  *   [n*stride_tok + h*head_dim + d] (stride in elements, >= Hk*head_dim).
  * slot_mapping: device int64[num_tokens]; negative entries are skipped.
