@@ -268,33 +268,29 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
 // Grid of the grid-stride store: every CTA takes the same number of tokens,
 // so the grid is the CTAs that fit on the device at once (one wave; a second
 // partial wave would finish last with a whole share each).  Resident CTAs
-// per SM are asked once per (device, kv heads) and kept.
-template <typename Kern>
-int store_grid(Kern kernel, int num_kv_heads, size_t smem, int num_tokens)
+// per SM are asked once per (instantiation, device, kv heads) and kept: the
+// instantiations differ in registers and so in CTAs per SM.
+template <typename T, bool KEY_FP8, int KBITS, int VBITS, bool NORM_CORR>
+cudaError_t launch_one(const StoreArgs& a, cudaStream_t st)
 {
+    auto kernel = store_kernel<T, KEY_FP8, KBITS, VBITS, NORM_CORR>;
     static std::atomic<int> cache[16][33];     // devices x kv heads: resident CTAs on the device
+    const int threads = 32 * a.num_kv_heads;
+    const size_t smem = size_t(a.num_kv_heads) * a.g.slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); dev = 0; }
-    int n = (dev >= 0 && dev < 16) ? cache[dev][num_kv_heads].load(std::memory_order_relaxed) : 0;
+    const bool keep = dev >= 0 && dev < 16;
+    int n = keep ? cache[dev][a.num_kv_heads].load(std::memory_order_relaxed) : 0;
     if (n <= 0) {
         int sms = 0, per_sm = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = kNumSMs;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * num_kv_heads, smem) != cudaSuccess ||
-            per_sm <= 0)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm <= 0)
             per_sm = 4;
         cudaGetLastError();
         n = sms * per_sm;
-        if (dev >= 0 && dev < 16) cache[dev][num_kv_heads].store(n, std::memory_order_relaxed);
+        if (keep) cache[dev][a.num_kv_heads].store(n, std::memory_order_relaxed);
     }
-    return num_tokens < n ? num_tokens : n;
-}
-
-template <typename Kern>
-cudaError_t launch_one(Kern kernel, const StoreArgs& a, cudaStream_t st)
-{
-    const int threads = 32 * a.num_kv_heads;
-    const size_t smem = size_t(a.num_kv_heads) * a.g.slot;
-    kernel<<<store_grid(kernel, a.num_kv_heads, smem, a.num_tokens), threads, smem, st>>>(a);
+    kernel<<<a.num_tokens < n ? a.num_tokens : n, threads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -302,11 +298,11 @@ template <typename T>
 cudaError_t launch_store_t(int preset, const StoreArgs& a, cudaStream_t st)
 {
     switch (preset & 0xFF) {
-    case TQ_K8V4:    return launch_one(store_kernel<T, true, 4, 4, false>, a, st);
-    case TQ_4BIT_NC: return launch_one(store_kernel<T, false, 4, 4, true>, a, st);
-    case TQ_K3V4_NC: return launch_one(store_kernel<T, false, 3, 4, true>, a, st);
-    case TQ_3BIT_NC: return launch_one(store_kernel<T, false, 3, 3, true>, a, st);
-    case TQ_2BIT_NC: return launch_one(store_kernel<T, false, 2, 2, true>, a, st);
+    case TQ_K8V4:    return launch_one<T, true, 4, 4, false>(a, st);
+    case TQ_4BIT_NC: return launch_one<T, false, 4, 4, true>(a, st);
+    case TQ_K3V4_NC: return launch_one<T, false, 3, 4, true>(a, st);
+    case TQ_3BIT_NC: return launch_one<T, false, 3, 3, true>(a, st);
+    case TQ_2BIT_NC: return launch_one<T, false, 2, 2, true>(a, st);
     default: return cudaErrorInvalidValue;
     }
 }
