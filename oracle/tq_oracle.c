@@ -262,25 +262,15 @@ static const double* orc_hadamard_cached(int D)
 
 /* ======================================================================
  * Bit packing.  [Atlas] "Background": 3-bit data is 8 values per 3 bytes;
- * 4-bit is two per byte, 2-bit four per byte.  The bit order is not on the
- * pages.  Readings used here:
- *  - 2, 4 and 8 bits: LSB-first, code i occupies bits [b*i, b*i + b) of the
- *    little-endian byte stream (4-bit: low nibble first).
- *  - 3 bits: groups of 32 codes in 12 bytes, read as three little-endian
- *    32-bit words W0, W1, W2.  For i = 0..7 and w = 0..2, bits [4i, 4i+3) of
- *    Ww hold code 8w + i, and bit 4i+3 of Ww holds bit w of code 24 + i.
- *    (Same density, 8 codes per 3 bytes; every code's low bits sit at a
- *    nibble boundary.)  n must be a multiple of 32.
+ * 4-bit is two per byte, 2-bit four per byte.  The bit order inside a byte
+ * group is not on the pages; the reading used here, for every width b:
+ * an LSB-first little-endian bitstream, code i occupying bits
+ * [b*i, b*i + b).  At 3 bits this makes every 3-byte group hold 8 whole
+ * codes (codes 8g..8g+7 in bytes 3g..3g+2); at 4 bits the low nibble comes
+ * first.
  * ==================================================================== */
 static void orc_setbit(uint8_t* out, int bit) { out[bit / 8] |= (uint8_t)(1u << (bit % 8)); }
 static int orc_getbit(const uint8_t* in, int bit) { return (in[bit / 8] >> (bit % 8)) & 1; }
-
-/* bit position (within the group's 96 bits) of bit j of code i, 3-bit layout */
-static int orc_bitpos3(int i, int j)
-{
-    if (i < 24) return 32 * (i / 8) + 4 * (i % 8) + j;
-    return 32 * j + 4 * (i - 24) + 3;
-}
 
 void orc_pack(const int* codes, int n, int bits, uint8_t* out)
 {
@@ -288,20 +278,14 @@ void orc_pack(const int* codes, int n, int bits, uint8_t* out)
     memset(out, 0, (size_t)nbytes);
     for (int i = 0; i < n; ++i)
         for (int j = 0; j < bits; ++j)
-            if ((codes[i] >> j) & 1) {
-                if (bits == 3) orc_setbit(out, 96 * (i / 32) + orc_bitpos3(i % 32, j));
-                else           orc_setbit(out, i * bits + j);
-            }
+            if ((codes[i] >> j) & 1) orc_setbit(out, i * bits + j);
 }
 
 void orc_unpack(const uint8_t* in, int n, int bits, int* codes)
 {
     for (int i = 0; i < n; ++i) {
         int c = 0;
-        for (int j = 0; j < bits; ++j) {
-            int bit = bits == 3 ? 96 * (i / 32) + orc_bitpos3(i % 32, j) : i * bits + j;
-            c |= orc_getbit(in, bit) << j;
-        }
+        for (int j = 0; j < bits; ++j) c |= orc_getbit(in, i * bits + j) << j;
         codes[i] = c;
     }
 }

@@ -76,8 +76,8 @@ void orc_signs(int D, uint64_t seed, int8_t* s);
 /* Normalised Sylvester Hadamard H[i][j] = (-1)^popcount(i&j) / sqrt(D). */
 void orc_hadamard(int D, double* H);
 
-/* ---- bit packing: 2/4/8 bits LSB-first (code i at bits [b*i, b*i+b));
- *      3 bits in 32-code groups of three 32-bit words (see tq_oracle.c) ---- */
+/* ---- bit packing: every width LSB-first, code i at bits [b*i, b*i+b) of
+ *      the little-endian byte stream (3 bits: 8 codes per 3 bytes) ---- */
 void orc_pack(const int* codes, int n, int bits, uint8_t* out);
 void orc_unpack(const uint8_t* in, int n, int bits, int* codes);
 

@@ -100,14 +100,26 @@ def test_iteration_cap_and_previous_iterate(orc):
 
 
 def test_page_constants(orc):
+    """The oracle runs with the constants the page's centroids.py prints:
+    its defaults are the golden file's panel count, iteration cap and
+    tolerance, and with no iteration it returns the page's start, the
+    centres of 2^b equal cells on [-3.5 sigma, 3.5 sigma]."""
+    import inspect
     vals = {}
     with open(__file__.replace("test_oracle_codebook.py", "golden/page_numbers.txt")) as f:
         for line in f:
             if line.strip() and not line.startswith("#"):
                 k, v = line.split()
                 vals[k] = float(v)
-    # the defaults of lloyd_max are the page's constants
-    a = orc.lloyd_max(128, 3)
-    b = orc.lloyd_max(128, 3, trapz_n=int(vals["lloyd_trapz_panels"]),
-                      max_iter=int(vals["lloyd_max_iter"]), tol=vals["lloyd_tol"])
-    assert np.array_equal(a[1], b[1])
+    defaults = inspect.signature(orc.lloyd_max).parameters
+    assert defaults["trapz_n"].default == vals["lloyd_trapz_panels"]
+    assert defaults["max_iter"].default == vals["lloyd_max_iter"]
+    assert defaults["tol"].default == vals["lloyd_tol"]
+    for d, bits in ((128, 3), (64, 2)):
+        sigma = 1 / math.sqrt(d)
+        half = vals["lloyd_init_range_sigmas"] * sigma
+        n = 1 << bits
+        c0, _, _, it = orc.lloyd_max(d, bits, max_iter=0)
+        assert it == 0
+        start = -half + 2 * half * (np.arange(n) + 0.5) / n
+        assert np.max(np.abs(c0 - start)) < 1e-15

@@ -1,7 +1,7 @@
 """Pins for the oracle's bit packing: byte examples worked out by hand for
-the LSB-first reading (2/4 bits) and the 32-code group reading (3 bits),
-round trips over every code value, and the packed sizes the pages give
-(8 values per 3 bytes at 3 bits)."""
+the LSB-first bitstream reading at every width, the 8-codes-per-3-bytes
+grouping the pages give for 3-bit data, round trips over every code value,
+and the packed sizes at head_dim 128."""
 import numpy as np
 import pytest
 
@@ -11,25 +11,30 @@ def test_worked_examples(orc):
     assert list(orc.pack([1, 2], 4)) == [0x21]
     # 2-bit codes 0..3 -> 0b11100100
     assert list(orc.pack([0, 1, 2, 3], 2)) == [0xE4]
-    # 3-bit group of 32: codes 0..7 in the nibbles of W0 (0x76543210), codes
-    # 8..23 likewise in W1, W2; code 24+i spreads its bits over the top bit of
-    # nibble i of W0, W1, W2.
-    codes = [0] * 32
-    for i in range(8):
-        codes[i] = i
-    assert list(orc.pack(codes, 3)) == [0x10, 0x32, 0x54, 0x76] + [0] * 8
-    codes = [0] * 32
-    codes[24] = 0b101          # bit 0 -> W0 bit 3, bit 2 -> W2 bit 3
-    codes[31] = 0b010          # bit 1 -> W1 bit 31
-    assert list(orc.pack(codes, 3)) == [0x08, 0, 0, 0, 0, 0, 0, 0x80, 0x08, 0, 0, 0]
-    # 8 three-bit values per 3 bytes ("turboquant-plus.md", Background)
-    assert orc.pack([7] * 32, 3).size == 12
+    # 3-bit codes 0..7, worked by hand: bit stream (LSB first)
+    #   000 100 010 110 001 101 011 111  ->  bytes 0b10001000, 0b11000110, 0b11111010
+    assert list(orc.pack(list(range(8)), 3)) == [0x88, 0xC6, 0xFA]
+    # a code that straddles a byte: code 2 = 0b101 sits in bits 6..8
+    assert list(orc.pack([0, 0, 5], 3)) == [0x40, 0x01]
+
+
+def test_three_bit_groups_of_three_bytes(orc):
+    """8 values per 3 bytes ("turboquant-plus.md", Background): every
+    3-byte group holds 8 whole codes, so group g depends on codes 8g..8g+7
+    only."""
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 8, 128)
+    data = orc.pack(codes, 3)
+    assert data.size == 48
+    for g in range(16):
+        alone = orc.pack(codes[8 * g:8 * g + 8], 3)
+        assert np.array_equal(data[3 * g:3 * g + 3], alone)
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4, 8])
 def test_round_trip(orc, bits):
     rng = np.random.default_rng(bits)
-    for n in ((32, 64, 128) if bits == 3 else (1, 7, 8, 128, 129)):
+    for n in (1, 7, 8, 32, 128, 129):
         codes = rng.integers(0, 1 << bits, n)
         data = orc.pack(codes, bits)
         assert data.size == (n * bits + 7) // 8

@@ -1,7 +1,10 @@
 """Pins for the oracle's rotation: the normalised Sylvester Hadamard matrix
 against scipy.linalg.hadamard, orthonormality and symmetry, the sign
-generator against published SplitMix64 outputs, and the round trip of the
-randomized Hadamard transform."""
+generator against published SplitMix64 outputs, the round trip of the
+randomized Hadamard transform, and the store's pre-quantisation coordinates
+for one-hot and two-hot keys, which fix the order "signs, then transform"
+("turboquant-plus.md", Background: a random sign vector followed by a
+Walsh-Hadamard transform)."""
 import os
 
 import numpy as np
@@ -46,3 +49,43 @@ def test_rht_round_trip_and_parseval(orc):
         assert abs(np.linalg.norm(y) - np.linalg.norm(x)) < 1e-12 * np.linalg.norm(x)
         back = s * (H @ y)
         assert np.max(np.abs(back - x)) < 1e-12 * np.linalg.norm(x)
+
+
+def _store_y(orc, k, preset=2):
+    L = orc.layout(preset)
+    s = orc.signs(128, 42)
+    c32, m32 = orc.codebook(128, L["key_bits"])
+    _, y = orc.store_one(preset, np.asarray(k, np.float32), np.zeros(128, np.float32), s, c32, m32)
+    return y.astype(np.float64), s.astype(np.float64)
+
+
+@pytest.mark.parametrize("j", [0, 1, 5, 64, 127])
+def test_store_rotation_one_hot(orc, j):
+    """k = a e_j gives y = H (s . k) / ||k|| = s_j H[:, j], with H from scipy
+    (not the oracle's own matrix).  Rotating first and flipping signs after
+    (s . H k) or leaving the signs out gives another vector for some j."""
+    H = sylvester(128) / np.sqrt(128)
+    k = np.zeros(128)
+    k[j] = 3.0
+    y, s = _store_y(orc, k)
+    want = s[j] * H[:, j]
+    assert np.max(np.abs(y - want)) < 1e-7
+    assert abs(np.linalg.norm(y) - 1) < 1e-6
+
+
+@pytest.mark.parametrize("i,j", [(0, 1), (3, 70), (12, 127)])
+def test_store_rotation_two_hot(orc, i, j):
+    """k = a e_i + b e_j: y = (a s_i H[:, i] + b s_j H[:, j]) / sqrt(a^2 + b^2).
+    With the sign vector's entries of opposite sign at i and j (checked), a
+    rotation taken in the other order, s . (H k) / ||k||, lands elsewhere."""
+    H = sylvester(128) / np.sqrt(128)
+    s = orc.signs(128, 42).astype(np.float64)
+    assert s[i] != s[j]
+    a, b = 2.0, -0.5
+    k = np.zeros(128)
+    k[i], k[j] = a, b
+    y, _ = _store_y(orc, k)
+    want = (a * s[i] * H[:, i] + b * s[j] * H[:, j]) / np.hypot(a, b)
+    assert np.max(np.abs(y - want)) < 1e-7
+    other = s * (H @ k) / np.hypot(a, b)
+    assert np.max(np.abs(other - want)) > 1e-2

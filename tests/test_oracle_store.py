@@ -175,3 +175,42 @@ def test_soa_store_is_a_rearrangement(orc, preset):
     o1, l1 = orc.decode_dense(preset, q, aos, bt, sl, Hk, bs, s, c32)
     o2, l2 = orc.decode_dense(preset | orc.LAYOUT_SOA, q, soa, bt, sl, Hk, bs, s, c32)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("preset,qmax", [(1, 15), (3, 7), (4, 3)])
+def test_value_code_ties_round_half_even(orc, preset, qmax):
+    """Exact half-integer quotients round to the even code (reading R9,
+    round-half-even): with min 0 and max qmax the fp16 scale is exactly 1
+    and the zero 0, so v itself is the quotient.  Worked by hand: 0.5 -> 0,
+    1.5 -> 2, 2.5 -> 2, and qmax - 0.5 -> the even neighbour; a round-half-up
+    rule would give 1, 2, 3 and qmax there."""
+    L, s, c32, m32 = _setup(orc, preset)
+    v = np.zeros(128, np.float32)
+    v[1] = qmax
+    ties = {2: 0.5, 3: 1.5, 4: 2.5, 5: qmax - 0.5}
+    for i, x in ties.items():
+        v[i] = x
+    k = np.random.default_rng(0).normal(size=128).astype(np.float32)
+    slot, _ = orc.store_one(preset, k, v, s, c32, m32)
+    u16 = lambda o: int(slot[o]) | int(slot[o + 1]) << 8
+    assert orc.f16_value(u16(L["off_v_scale"])) == 1.0
+    assert orc.f16_value(u16(L["off_v_zero"])) == 0.0
+    codes = orc.unpack(slot[L["off_v_data"]:L["off_v_data"] + L["value_data_bytes"]], 128,
+                       L["value_bits"])
+    even = lambda x: int(np.floor(x)) if int(np.floor(x)) % 2 == 0 else int(np.floor(x)) + 1
+    assert codes[1] == qmax
+    for i, x in ties.items():
+        assert codes[i] == even(x), (i, x, codes[i])
+    assert [codes[i] for i in (2, 3, 4)] == [0, 2, 2]
+
+
+def test_value_code_ties_scaled(orc):
+    """The same rule through a non-unit scale: 4-bit values on [0, 7.5] give
+    scale 0.5 (exact in fp16), so v = 1.25 and 1.75 are quotients 2.5 and
+    3.5 and take codes 2 and 4."""
+    L, s, c32, m32 = _setup(orc, 1)
+    v = np.zeros(128, np.float32)
+    v[1], v[2], v[3] = 7.5, 1.25, 1.75
+    slot, _ = orc.store_one(1, np.ones(128, np.float32), v, s, c32, m32)
+    codes = orc.unpack(slot[L["off_v_data"]:L["off_v_data"] + 64], 128, 4)
+    assert list(codes[1:4]) == [15, 2, 4]
