@@ -46,9 +46,9 @@ struct DecodeArgs {
 constexpr int kWarps = 4;
 
 // Codes 4*lane .. 4*lane+3 of a packed code stream starting at p (2-byte
-// aligned).  4 bits: low nibble first.  2 bits: four per byte, LSB first.
-// 3 bits: 32-code groups of three 32-bit words W0..W2, code 8w+i in bits
-// [4i, 4i+3) of Ww, bit w of code 24+i in bit 4i+3 of Ww.
+// aligned).  Every width is an LSB-first bitstream: 4 bits low nibble first,
+// 2 bits four per byte, 3 bits 8 codes per 3 bytes (the lane's 12 bits start
+// at bit 12*lane, i.e. byte 3*lane/2 plus 0 or 4 bits).
 template <int BITS>
 __device__ __forceinline__ void load_codes(const uint8_t* p, int lane, int (&c)[4])
 {
@@ -62,20 +62,10 @@ __device__ __forceinline__ void load_codes(const uint8_t* p, int lane, int (&c)[
         for (int i = 0; i < 4; ++i) c[i] = (w >> (4 * i)) & 15u;
     } else {
         static_assert(BITS == 3, "2, 3 or 4 bits");
-        const int j = lane & 7;
-        const uint8_t* g = p + 12 * (lane >> 3);
-        if (j < 6) {
-            const uint32_t w = ld_u16(g + 4 * (j >> 1) + 2 * (j & 1));
+        const uint8_t* q = p + ((3 * lane) >> 1);
+        const uint32_t w = (uint32_t(q[0]) | uint32_t(q[1]) << 8) >> (4 * (lane & 1));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c[i] = (w >> (4 * i)) & 7u;
-        } else {
-            const int h = j - 6;
-            const uint32_t w0 = ld_u16(g + 2 * h), w1 = ld_u16(g + 4 + 2 * h), w2 = ld_u16(g + 8 + 2 * h);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                c[i] = ((w0 >> (4 * i + 3)) & 1u) | (((w1 >> (4 * i + 3)) & 1u) << 1) |
-                       (((w2 >> (4 * i + 3)) & 1u) << 2);
-        }
+        for (int i = 0; i < 4; ++i) c[i] = (w >> (3 * i)) & 7u;
     }
 }
 

@@ -72,7 +72,8 @@ float two_bit_alpha()
 // Launch geometry shared by the launcher and the occupancy query.
 struct MmaGeom {
     int hpc, copy_bytes, smem_row, meta_bytes, nstages;
-    size_t smem;
+    size_t smem;          // dynamic shared memory
+    size_t static_smem;   // the kernel's own: the 3-bit keys' pair table
 };
 
 MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G)
@@ -92,9 +93,11 @@ MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G)
     m.smem_row = (m.copy_bytes % 32 == 0) ? m.copy_bytes + 16 : m.copy_bytes;
     const int stage = kTile * (m.smem_row + m.meta_bytes);
     // ring budget: two CTAs of Hk warps, or four CTAs of 4 warps, per SM;
-    // MSE keys with G = 8 also keep 4 KB of q fragments per warp
+    // MSE keys with G = 8 also keep 4 KB of q fragments per warp, and 3-bit
+    // keys hold their 8 KB pair table in static shared memory
     const int qsm = (!L.key_fp8 && G > 4) ? m.hpc * 4096 : 0;
-    int nst = ((m.hpc < Hk ? 56 * 1024 : 100 * 1024) + (qsm ? 12 * 1024 : 0) - qsm) / stage;
+    m.static_smem = (!L.key_fp8 && L.key_bits == 3) ? size_t(kLut3Entries) * 8 : 0;
+    int nst = ((m.hpc < Hk ? 56 * 1024 : 100 * 1024) + (qsm ? 12 * 1024 : 0) - qsm - int(m.static_smem)) / stage;
     nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
     // the q staging at kernel start borrows the ring: hpc * (4 or 8) heads * 512 B
     while (nst * stage < m.hpc * (G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
@@ -147,7 +150,7 @@ void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group,
     if (n <= 0) {
         // no device to ask: a GB300 SM's 228 KB of shared memory (1 KB kept
         // per CTA) and 64K registers at 128 per thread
-        const int by_smem = int((228 * 1024) / (m.smem + 1024));
+        const int by_smem = int((228 * 1024) / (m.smem + m.static_smem + 1024));
         const int by_regs = 65536 / (128 * 32 * m.hpc);
         n = (by_smem < by_regs ? by_smem : by_regs) * kNumSMs;
     }

@@ -21,6 +21,9 @@
 // part).  FP8 keys and integer value codes are exact in fp16.  The value
 // path uses P' = p * v_scale and adds sum_t p_t v_zero_t separately
 // (v_hat = code * scale + zero).
+// Centroid lookups: 3-bit keys read code pairs from a shared-memory table
+// (one 8-byte load per pair: both centroids, hi and lo); 2- and 4-bit keys
+// select bytes of register tables with PRMT.
 //
 // Launch chain: stage 1 is a programmatic dependent of the previous kernel
 // in the stream and waits for it before its first global read; stage 2 is a
@@ -174,14 +177,41 @@ __device__ __forceinline__ float lds_f16(const uint8_t* p)
     return __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(p)));
 }
 
-// 3-bit group (32 codes in words W0..W2): nibble words of codes 0-7, 8-15,
-// 16-23, 24-31 with every nibble's top bit clear.
-__device__ __forceinline__ void nibbles3(const uint32_t (&w)[3], uint32_t (&n)[4])
+// Eight 3-bit codes (bits 0..23 of x, code i at bit 3i) spread to a nibble
+// word (code i in bits [4i, 4i+3), every nibble's top bit clear).  Each
+// step moves the upper part of every field up with a masked multiply-add:
+// a + (2^k - 1) * (a & m) = (a & ~m) + 2^k (a & m).
+__device__ __forceinline__ uint32_t spread3(uint32_t x)
 {
-    n[0] = w[0] & 0x77777777u;
-    n[1] = w[1] & 0x77777777u;
-    n[2] = w[2] & 0x77777777u;
-    n[3] = ((w[0] >> 3) & 0x11111111u) | ((w[1] >> 2) & 0x22222222u) | ((w[2] >> 1) & 0x44444444u);
+    uint32_t a = x & 0x00FFFFFFu;
+    a += 15u * (a & 0x00FFF000u);     // codes 4..7 to bits 16..27
+    a += 3u * (a & 0x0FC00FC0u);      // codes 2, 3 (6, 7) up by 2 bits: two codes per byte
+    a += a & 0x38383838u;             // odd codes up by 1 bit
+    return a;
+}
+
+// 3-bit keys: a code pair (codes 2p, 2p + 1 of a 32-code group, the 6-bit
+// field at bit 6p of the group's 96-bit LSB-first stream w[0..2]) indexes a
+// shared table of 64 entries, each the pair's (hi, lo) fp16x2 centroids.
+// Entries are 128 bytes apart and hold one copy per half-warp lane (lane
+// & 15 at byte 8 (lane & 15)), so the 16 lanes of each half of an 8-byte
+// load touch 16 distinct bank pairs whatever codes they read.  The field is
+// shifted to bits [7, 13), the entry offset.
+constexpr int kLut3Entries = 64 * 16;
+
+__device__ __forceinline__ uint32_t pair_off(const uint32_t (&w)[3], int bit)
+{
+    const int wi = bit >> 5, b = bit & 31;
+    uint32_t x;
+    if (b + 6 > 32)  x = __funnelshift_r(w[wi], w[wi + 1], b - 7);
+    else if (b >= 7) x = w[wi] >> (b - 7);
+    else             x = w[wi] << (7 - b);
+    return x & 0x1F80u;
+}
+
+__device__ __forceinline__ uint2 lut_pair(const uint2* lut, const uint32_t (&w)[3], int p, uint32_t l8)
+{
+    return *reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(lut) + (pair_off(w, 6 * p) | l8));
 }
 
 // Longest-first dispatch: CTA row y (blockIdx.y) takes the sequence of rank y
@@ -283,8 +313,8 @@ __device__ __forceinline__ void lut16_sym(const uint32_t (&T)[8][2], uint32_t s,
 template <int KMODE, int G, bool KGEN, int KM, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
-                                        const uint4* qsm, const uint32_t (&T)[NT][2], float (&out)[4],
-                                        float (&outl)[4])
+                                        const uint4* qsm, const uint32_t (&T)[NT][2], const uint2* lut,
+                                        uint32_t l8, float (&out)[4], float (&outl)[4])
 {
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float scl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -299,17 +329,35 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
             mma16816(sc[kk & 1], A, bq[kk][0], bq[kk][1]);
             if constexpr (G == 8) mma16816(scl[kk & 1], A, bql[kk][0], bql[kk][1]);
         }
+    } else if constexpr (KMODE == 3) {
+        // the thread's 32 codes of each row (dims 32 tig .. 32 tig + 31, 12
+        // bytes); k-step kk takes pairs 2 kk (A columns 2 tig, 2 tig + 1) and
+        // 2 kk + 1 (columns 2 tig + 8, 2 tig + 9); one table load gives a
+        // pair's hi and lo words
+        uint32_t w0[3], w1[3];
+        lds_words<3, KM>(r0 + 12 * tig, kmis, w0);
+        lds_words<3, KM>(r1 + 12 * tig, kmis, w1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint2 e00 = lut_pair(lut, w0, 2 * kk, l8), e01 = lut_pair(lut, w0, 2 * kk + 1, l8);
+            const uint2 e10 = lut_pair(lut, w1, 2 * kk, l8), e11 = lut_pair(lut, w1, 2 * kk + 1, l8);
+            const uint32_t Ahi[4] = {e00.x, e10.x, e01.x, e11.x};
+            const uint32_t Alo[4] = {e00.y, e10.y, e01.y, e11.y};
+            if constexpr (G == 4) {
+                mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
+                mma16816(sc[1], Alo, bq[kk][0], bq[kk][1]);
+            } else {
+                const uint4 qf = qsm[32 * kk];      // q hi (x, y) and lo (z, w) of this k-step
+                mma16816(sc[kk & 1], Ahi, qf.x, qf.y);
+                mma16816(scl[0], Ahi, qf.z, qf.w);
+                mma16816(scl[1], Alo, qf.x, qf.y);
+            }
+        }
     } else {
-        // one 32-code group (3-bit: 12 bytes, 4-bit: 16 bytes) of each row per
+        // one 32-code group (4-bit: 16 bytes, 2-bit: 8 bytes) of each row per
         // thread, as four nibble words of 8 codes (k-step kk uses 4 of them)
         uint32_t c0[4], c1[4];
-        if constexpr (KMODE == 3) {
-            uint32_t w0[3], w1[3];
-            lds_words<3, KM>(r0 + 12 * tig, kmis, w0);
-            lds_words<3, KM>(r1 + 12 * tig, kmis, w1);
-            nibbles3(w0, c0);
-            nibbles3(w1, c1);
-        } else if constexpr (KMODE == 2) {
+        if constexpr (KMODE == 2) {
             // 32 two-bit codes = two words; the even codes of a word go to one
             // nibble word and the odd codes to another (code 2i / 2i + 1 of
             // the word in nibble i), so k-step kk covers dims with stride 2
@@ -340,7 +388,7 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
                 lut16_sym(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
                 lut16_sym(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
             } else {
-                // 2- and 3-bit keys: one lookup per byte plane, then interleave
+                // 2-bit keys: one lookup per byte plane, then interleave
                 // the low and high bytes into half2 registers
                 const uint32_t p0 = prmt(T[0][0], T[0][1], s0), p1 = prmt(T[1][0], T[1][1], s0);
                 const uint32_t q0 = prmt(T[0][0], T[0][1], s1), q1 = prmt(T[1][0], T[1][1], s1);
@@ -443,11 +491,15 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
             vw[j][0] = w[0];
             vw[j][1] = 0u;
         } else {
-            uint32_t w[3], n[4];
-            lds_words<3, VM>(rv + 12 * (gid >> 1), vmis, w);
-            nibbles3(w, n);
-            vw[j][0] = (gid & 1) ? n[2] : n[0];
-            vw[j][1] = (gid & 1) ? n[3] : n[1];
+            // 3 bits: dims 16 gid .. 16 gid + 15 are the 48 bits from byte
+            // 6 gid, inside the two aligned words from 6 gid - m (m = its
+            // misalignment, 0 or 2); spread to two nibble words
+            const int m = ((VM >= 0 ? VM : vmis) + 2 * (gid & 1)) & 2;
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(rv + 6 * gid - m);
+            const uint32_t x0 = q[0], x1 = q[1];
+            const uint32_t lo = __funnelshift_r(x0, x1, 8 * m), hi = x1 >> (8 * m);
+            vw[j][0] = spread3(lo);
+            vw[j][1] = spread3(__funnelshift_r(lo, hi, 24));
         }
     }
     // MMAs i and i + 1 (dims 16 gid + 2i .. 2i + 3) share one byte gather:
@@ -506,6 +558,8 @@ template <typename TQ, int KMODE, int VBITS, int G, bool SOA, bool SPARSE>
 __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
+    // 3-bit keys: the code-pair centroid table (8 KB; one element elsewhere)
+    __shared__ __align__(16) uint2 key_lut[KMODE == 3 ? kLut3Entries : 1];
     // launched as a programmatic dependent of the previous kernel in the
     // stream (typically the store of the step's new tokens): wait for it to
     // complete before the first read of global memory
@@ -661,6 +715,19 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         if (err <= 5e-7f) { key_alpha = al; key_lo = false; }
     }
 
+    // 3-bit keys: entry e (codes e & 7 and e >> 3) of the pair table holds
+    // fp16x2 (hi) and fp16x2 (lo) of the two centroids, once per half-warp
+    // lane; the barrier after the q staging below orders it before any use
+    if constexpr (KMODE == 3) {
+        for (int i = threadIdx.x; i < kLut3Entries; i += blockDim.x) {
+            const int e = i >> 4;
+            float h0, l0, h1, l1;
+            split_f16(a.centroids[e & 7], h0, l0);
+            split_f16(a.centroids[e >> 3], h1, l1);
+            key_lut[i] = make_uint2(pack_half2(h0, h1), pack_half2(l0, l1));
+        }
+    }
+
     // MSE keys with G = 8 keep their q fragments in shared memory after the
     // ring's barriers (4 KB per warp, read once per k-step) instead of 32
     // registers: the register file is the limit of that instantiation.
@@ -728,10 +795,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     if (warp == 0)
         for (int i = s_q; i < NST; ++i) issue(i, i);
 
-    // ---------------- centroid byte planes for the PRMT lookup (MSE keys):
-    // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
-    // fp16 residual c - fp16(c), with c = key_alpha * c_k.  2- and 3-bit keys: T[p][k >> 2] holds entries
-    // 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
+    // ---------------- centroid byte planes for the PRMT lookup (2- and 4-bit
+    // keys): plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte
+    // of the fp16 residual c - fp16(c), with c = key_alpha * c_k.  2-bit keys:
+    // T[p][k >> 2] holds entries 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
     // plane p of codes 8(k>>3) .. 8(k>>3)+7 in the same way.
     // 4-bit keys with a symmetric codebook (c_k = -c_(15-k) bit for bit; the
     // same test in every thread) use the 8-entry magnitude planes instead.
@@ -755,7 +822,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             T[2][w] |= (lb & 0xFFu) << sh;
             T[3][w] |= (lb >> 8) << sh;
         }
-    } else if constexpr (KMODE != 8) {
+    } else if constexpr (KMODE == 2 || KMODE == 4) {
         constexpr int NC = 1 << KMODE;
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
@@ -782,6 +849,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
     const int tau0 = gid, tau1 = gid + 8;      // this thread's QK rows
+    const uint32_t l8 = uint32_t(lane & 15) * 8;   // this lane's copy in a pair-table entry
     const int hoff = warp * int(hs_g);         // this warp's slot (SoA: data record) in a shared row
     const int kmis = hoff & 2;
     const int vmis = (hoff + a.g.v_off) & 2;
@@ -810,7 +878,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
-            qk_tile<KMODE, G, KGEN, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, sc, scl);
+            qk_tile<KMODE, G, KGEN, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, key_lut, l8, sc, scl);
             float n0 = 1.f, n1 = 1.f;
             if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
             vs[rt][0] = lds_f16(m0 + a.g.m_scale);

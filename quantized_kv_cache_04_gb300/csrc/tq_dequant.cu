@@ -32,12 +32,14 @@ struct DqArgs {
 
 constexpr int kDqWarps = 8;           // warps per CTA, one token at a time each
 
-// Raw packed codes of the lane's 4 dims: 4-bit: one 16-bit word; 3-bit: the
-// lane's 32-code group as three 32-bit words.  Loaded in a first phase so
-// that the loads of several pairs are in flight together.
+// Raw packed codes of the lane's 4 dims (every width an LSB-first
+// bitstream): 4-bit: one 16-bit word; 2-bit: one byte; 3-bit: the 16 bits
+// from byte 3*lane/2, whose low 12 (lane even) or high 12 (lane odd) bits
+// are the lane's codes.  Loaded in a first phase so that the loads of
+// several pairs are in flight together.
 template <int BITS>
 struct RawCodes {
-    uint32_t w[BITS == 3 ? 3 : 1];
+    uint32_t w[1];
 };
 
 template <int BITS>
@@ -48,17 +50,12 @@ __device__ __forceinline__ void load_codes(const uint8_t* p, int lane, RawCodes<
     } else if constexpr (BITS == 4) {
         r.w[0] = ld_u16(p + 2 * lane);
     } else {
-        const uint8_t* grp = p + 12 * (lane >> 3);
-#pragma unroll
-        for (int w = 0; w < 3; ++w)
-            r.w[w] = uint32_t(ld_u16(grp + 4 * w)) | (uint32_t(ld_u16(grp + 4 * w + 2)) << 16);
+        const uint8_t* q = p + ((3 * lane) >> 1);
+        r.w[0] = uint32_t(q[0]) | (uint32_t(q[1]) << 8);
     }
 }
 
-// Codes of dims 4 lane .. 4 lane + 3.  2-bit: four per byte, LSB first.
-// 4-bit: low nibble first.  3-bit:
-// groups of 32 codes in 12 bytes read as words W0..W2; code 8w + i sits in
-// bits 4i..4i+2 of Ww, and bit w of code 24 + i in bit 4i + 3 of Ww.
+// Codes of dims 4 lane .. 4 lane + 3.
 template <int BITS>
 __device__ __forceinline__ void lane_codes(const RawCodes<BITS>& r, int lane, int (&c)[4])
 {
@@ -69,19 +66,9 @@ __device__ __forceinline__ void lane_codes(const RawCodes<BITS>& r, int lane, in
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[i] = (r.w[0] >> (4 * i)) & 15;
     } else {
-        const int j0 = 4 * (lane & 7);          // first code of the lane within its group
-        if (j0 < 24) {
-            const uint32_t wj = j0 < 8 ? r.w[0] : (j0 < 16 ? r.w[1] : r.w[2]);
-            const uint32_t x = wj >> (4 * (j0 & 7));
+        const uint32_t x = r.w[0] >> (4 * (lane & 1));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c[i] = (x >> (4 * i)) & 7;
-        } else {
-            const int sh = 4 * (j0 - 24) + 3;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                c[i] = int(((r.w[0] >> (sh + 4 * i)) & 1) | (((r.w[1] >> (sh + 4 * i)) & 1) << 1) |
-                           (((r.w[2] >> (sh + 4 * i)) & 1) << 2));
-        }
+        for (int i = 0; i < 4; ++i) c[i] = (x >> (3 * i)) & 7;
     }
 }
 

@@ -2,9 +2,10 @@
 //
 // Method: "turboquant-plus.md" (Atlas TQ+), section "Background" (randomised
 // Hadamard rotation, Lloyd-Max codebook, matched-norm L2 scale, 3-bit packing
-// of 8 codes per 3 bytes); "vllm.v1.attention.backends.turboquant_attn" API
-// page, sections "_store_kv" and "do_kv_cache_update" (fused store of K and V
-// into one slot per (block, token, kv head)).
+// of 8 codes per 3 bytes; every code stream is LSB-first);
+// "vllm.v1.attention.backends.turboquant_attn" API page, sections "_store_kv"
+// and "do_kv_cache_update" (fused store of K and V into one slot per (block,
+// token, kv head)).
 //
 // Mapping: one CTA per token (grid-stride), one warp per kv head, 4 consecutive
 // coordinates per lane.  The rotation is a warp-shuffle Walsh-Hadamard
@@ -79,21 +80,14 @@ __device__ __forceinline__ void pack_codes(uint8_t* dst, const int (&c)[4], int 
         const uint32_t hi = __shfl_down_sync(0xffffffffu, w, 1);
         if (!(lane & 1)) d16[lane >> 1] = uint16_t(w | (hi << 8));
     } else {
-        // 3 bits, 32-code groups of three 32-bit words W0..W2: code 8w+i in
-        // bits [4i, 4i+3) of Ww (i < 8, w < 3), bit w of code 24+i in bit
-        // 4i+3 of Ww.  Lanes 8g..8g+7 hold group g; lanes 8g+6, 8g+7 hold
-        // codes 24..31, whose bits ride in the nibble tops written by lanes
-        // 8g..8g+5 (lane 8g+2w+h writes half h of Ww).
+        // 3 bits: lanes 4g..4g+3 hold codes 16g..16g+15, 48 bits = three
+        // aligned 16-bit words at word 3g; lane 4g+j (j < 3) writes word j,
+        // bits [16j, 16j+16) of the group, from its own 12 bits and the next
+        // lane's
         static_assert(BITS == 3, "2, 3 or 4 bits");
-        const int j = lane & 7, h = j & 1, w3 = j >> 1;
-        const uint32_t spill = __shfl_sync(0xffffffffu, w, (lane & ~7) + 6 + h);
-        if (j < 6) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                v |= ((uint32_t(c[i]) & 7u) | (((spill >> (3 * i + w3)) & 1u) << 3)) << (4 * i);
-            d16[6 * (lane >> 3) + 2 * w3 + h] = uint16_t(v);
-        }
+        const uint32_t nxt = __shfl_down_sync(0xffffffffu, w, 1);
+        const int j = lane & 3;
+        if (j < 3) d16[3 * (lane >> 2) + j] = uint16_t((w >> (4 * j)) | (nxt << (12 - 4 * j)));
     }
 }
 
