@@ -330,29 +330,51 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
             if constexpr (G == 8) mma16816(scl[kk & 1], A, bql[kk][0], bql[kk][1]);
         }
     } else if constexpr (KMODE == 3) {
-        // the thread's 32 codes of each row (dims 32 tig .. 32 tig + 31, 12
-        // bytes); k-step kk takes pairs 2 kk (A columns 2 tig, 2 tig + 1) and
-        // 2 kk + 1 (columns 2 tig + 8, 2 tig + 9); one table load gives a
-        // pair's hi and lo words
+        // 3-bit keys: the MMA's 16 rows are 8 tokens x {hi, lo}: row gid
+        // holds token gid's fp16 centroids, row gid + 8 their fp16
+        // residuals, so one table load (a code pair's hi and lo words) is
+        // A registers a0 / a1 (pair 2 kk, columns 2 tig, 2 tig + 1) or a2 / a3
+        // (pair 2 kk + 1, columns 2 tig + 8, 2 tig + 9) as loaded.  The
+        // thread's two tokens (rows r0, r1; the thread's 32 codes of each,
+        // dims 32 tig .. 32 tig + 31, are 12 bytes) run as two such MMAs per
+        // k-step, and a token's score is the sum of its hi and lo rows.
         uint32_t w0[3], w1[3];
         lds_words<3, KM>(r0 + 12 * tig, kmis, w0);
         lds_words<3, KM>(r1 + 12 * tig, kmis, w1);
+        constexpr int NC = G == 4 ? 2 : 1;    // accumulator chains per token and q part
+        float c0[NC][4] = {}, c1[NC][4] = {}, d0[4] = {}, d1[4] = {};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const uint2 e00 = lut_pair(lut, w0, 2 * kk, l8), e01 = lut_pair(lut, w0, 2 * kk + 1, l8);
-            const uint2 e10 = lut_pair(lut, w1, 2 * kk, l8), e11 = lut_pair(lut, w1, 2 * kk + 1, l8);
-            const uint32_t Ahi[4] = {e00.x, e10.x, e01.x, e11.x};
-            const uint32_t Alo[4] = {e00.y, e10.y, e01.y, e11.y};
-            if constexpr (G == 4) {
-                mma16816(sc[0], Ahi, bq[kk][0], bq[kk][1]);
-                mma16816(sc[1], Alo, bq[kk][0], bq[kk][1]);
-            } else {
-                const uint4 qf = qsm[32 * kk];      // q hi (x, y) and lo (z, w) of this k-step
-                mma16816(sc[kk & 1], Ahi, qf.x, qf.y);
-                mma16816(scl[0], Ahi, qf.z, qf.w);
-                mma16816(scl[1], Alo, qf.x, qf.y);
+            const uint2 e0 = lut_pair(lut, w0, 2 * kk, l8), e1 = lut_pair(lut, w0, 2 * kk + 1, l8);
+            const uint2 f0 = lut_pair(lut, w1, 2 * kk, l8), f1 = lut_pair(lut, w1, 2 * kk + 1, l8);
+            const uint32_t A0[4] = {e0.x, e0.y, e1.x, e1.y};
+            const uint32_t A1[4] = {f0.x, f0.y, f1.x, f1.y};
+            if constexpr (G == 4) {            // columns: head x {q hi, q lo}
+                mma16816(c0[kk & 1], A0, bq[kk][0], bq[kk][1]);
+                mma16816(c1[kk & 1], A1, bq[kk][0], bq[kk][1]);
+            } else {                           // columns: 8 heads; q hi and q lo in two MMAs
+                const uint4 qf = qsm[32 * kk];
+                mma16816(c0[0], A0, qf.x, qf.y);
+                mma16816(c1[0], A1, qf.x, qf.y);
+                mma16816(d0, A0, qf.z, qf.w);
+                mma16816(d1, A1, qf.z, qf.w);
             }
         }
+        // out / outl in the layout of the 16-token form: [0] / [1] = token r0,
+        // columns 2 tig / 2 tig + 1; [2] / [3] = token r1
+#pragma unroll
+        for (int j = 1; j < NC; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { c0[0][i] += c0[j][i]; c1[0][i] += c1[j][i]; }
+        out[0] = c0[0][0] + c0[0][2];
+        out[1] = c0[0][1] + c0[0][3];
+        out[2] = c1[0][0] + c1[0][2];
+        out[3] = c1[0][1] + c1[0][3];
+        outl[0] = d0[0] + d0[2];
+        outl[1] = d0[1] + d0[3];
+        outl[2] = d1[0] + d1[2];
+        outl[3] = d1[1] + d1[3];
+        return;
     } else {
         // one 32-code group (4-bit: 16 bytes, 2-bit: 8 bytes) of each row per
         // thread, as four nibble words of 8 codes (k-step kk uses 4 of them)
