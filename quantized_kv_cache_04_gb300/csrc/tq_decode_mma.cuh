@@ -449,6 +449,50 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
     }
 }
 
+// 3-bit keys, both 16-row tiles at once: the four tokens of the thread
+// (rows r[0..3] = tokens gid, gid + 8 of tile 0, then of tile 1) in one
+// k-step loop, so the lookups and MMAs of the two tiles interleave.
+// out[rt] / outl[rt] as qk_tile's.
+template <int G, int KM>
+__device__ __forceinline__ void qk_tile3x2(const uint8_t* const (&r)[4], int tig, int kmis,
+                                           const uint32_t (&bq)[8][2], const uint4* qsm, const uint2* lut,
+                                           uint32_t l8, float (&out)[2][4], float (&outl)[2][4])
+{
+    uint32_t w[4][3];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lds_words<3, KM>(r[i] + 12 * tig, kmis, w[i]);
+    float c[4][4] = {}, d[4][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint4 qf;
+        if constexpr (G == 8) qf = qsm[32 * kk];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint2 e0 = lut_pair(lut, w[i], 2 * kk, l8), e1 = lut_pair(lut, w[i], 2 * kk + 1, l8);
+            const uint32_t A[4] = {e0.x, e0.y, e1.x, e1.y};
+            if constexpr (G == 4) {
+                mma16816(c[i], A, bq[kk][0], bq[kk][1]);
+            } else {
+                mma16816(c[i], A, qf.x, qf.y);
+                mma16816(d[i], A, qf.z, qf.w);
+            }
+        }
+    }
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt) {
+        const float (&c0)[4] = c[2 * rt], (&c1)[4] = c[2 * rt + 1];
+        const float (&d0)[4] = d[2 * rt], (&d1)[4] = d[2 * rt + 1];
+        out[rt][0] = c0[0] + c0[2];
+        out[rt][1] = c0[1] + c0[3];
+        out[rt][2] = c1[0] + c1[2];
+        out[rt][3] = c1[1] + c1[3];
+        outl[rt][0] = d0[0] + d0[2];
+        outl[rt][1] = d0[1] + d0[3];
+        outl[rt][2] = d1[0] + d1[2];
+        outl[rt][3] = d1[1] + d1[3];
+    }
+}
+
 // P' of one 16-row tile to the B layout of the value MMA: thread (gid, tig)
 // feeds column gid for tokens 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9
 // (b1), which QK threads with gid 2 tig and 2 tig + 1 hold (rows gid, gid + 8).
@@ -893,6 +937,12 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         // ---- scores of both 16-row tiles
         float s[NH][2][2], vs[2][2], vz[2][2];
         bool ok[2][2];
+        float sc2[2][4], scl2[2][4];
+        if constexpr (KMODE == 3) {
+            const uint8_t* const rr[4] = {st + tau0 * rs, st + tau1 * rs, st + (16 + tau0) * rs,
+                                          st + (16 + tau1) * rs};
+            qk_tile3x2<G, KM>(rr, tig, kmis, bq, qsm, key_lut, l8, sc2, scl2);
+        }
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt) {
             const uint8_t* r0 = st + (16 * rt + tau0) * rs;
@@ -900,7 +950,12 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
-            qk_tile<KMODE, G, KGEN, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, key_lut, l8, sc, scl);
+            if constexpr (KMODE == 3) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { sc[i] = sc2[rt][i]; scl[i] = scl2[rt][i]; }
+            } else {
+                qk_tile<KMODE, G, KGEN, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, key_lut, l8, sc, scl);
+            }
             float n0 = 1.f, n1 = 1.f;
             if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
             vs[rt][0] = lds_f16(m0 + a.g.m_scale);
@@ -1023,10 +1078,13 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             __syncwarp();
             int last = 0;
             if (lane == 0) {
-                __threadfence_block();
-                last = atomicAdd(&done[stage], 1) == nwarps - 1;
+                // release: this warp's reads of the stage come before the
+                // count; acquire: the last warp's refill comes after all
+                uint32_t prev;
+                asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                             : "=r"(prev) : "r"(smem_u32(&done[stage])) : "memory");
+                last = prev == uint32_t(nwarps - 1);
                 if (last) done[stage] = 0;
-                __threadfence_block();
             }
             if (__shfl_sync(0xffffffffu, last, 0)) issue(it + NST, stage);
             if (++stage == NST) { stage = 0; parity ^= 1u; }
