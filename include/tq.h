@@ -282,9 +282,10 @@ int tq_decode_attention_sparse_v(int preset, int head_dim, int batch, int num_q_
  * tq_decode_pick_splits does, lowered until B*Hq*S*(D+1)*4 bytes fit; an
  * explicit num_splits whose partials exceed the array returns
  * TQ_ERR_WORKSPACE, as does a shape for which even one split does not fit.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the one array and leave the
+ * Every call looks up the array's device address in the current device's
+ * context (cudaGetSymbolAddress); the first call on a device may load the
+ * library's device code there, so make that first call before any stream
+ * capture.  All calls share the one array and leave the
  * last call's partials in it (nothing in it has to start at zero): calls
  * whose kernels overlap on the GPU, e.g. on two streams at once, race. */
 #define TQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

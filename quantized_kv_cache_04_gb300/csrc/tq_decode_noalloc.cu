@@ -10,8 +10,6 @@
 #include "tq.h"
 #include "tq_internal.h"
 
-#include <mutex>
-
 namespace {
 
 // The split partials (fp32 [batch][q heads][splits][head_dim + 1]).  Every GPU
@@ -19,10 +17,6 @@ namespace {
 // process exits.  Its name is only a host-side stand-in: host code must use
 // the device address from cudaGetSymbolAddress.
 static __device__ __align__(256) float tq_noalloc_scratch[TQ_NOALLOC_SCRATCH_BYTES / sizeof(float)];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch[kMaxDevices];   // device address of the array, per device, found on first use
 
 }  // namespace
 
@@ -35,17 +29,15 @@ extern "C" int tq_decode_attention_noalloc(int preset, int head_dim, int batch, 
                                            const int8_t* signs, const float* centroids, void* out,
                                            int out_dtype, float* lse, void* stream)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TQ_ERR_CUDA;
+    // The array's address in the current device's context, looked up on
+    // every call: an address kept from an earlier call could belong to
+    // another context (after cudaDeviceReset, or under a driver-API context
+    // that is not the primary one).  Once the library's device code is
+    // loaded in the context this is a host-side table lookup.
     void* scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_scratch[dev]) {        // once per device, with that device current
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, tq_noalloc_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
-            g_scratch[dev] = p;
-        }
-        scratch = g_scratch[dev];
+    if (cudaGetSymbolAddress(&scratch, tq_noalloc_scratch) != cudaSuccess || !scratch) {
+        cudaGetLastError();
+        return TQ_ERR_CUDA;
     }
 
     // With num_splits = 0 the library's pick is lowered until the partials

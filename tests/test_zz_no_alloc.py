@@ -19,9 +19,12 @@ from quantized_kv_cache_04_gb300 import _lib
 pytestmark = pytest.mark.gpu
 
 
-def _problem(seed, preset, B, Hq, Hk, bs, ctx, dtype):
+def _problem(seed, preset, B, Hq, Hk, bs, ctx, dtype, on_device=False):
+    """A paged cache of B sequences of ctx tokens.  Inputs are drawn on the
+    CPU, or on the GPU for the large shapes (on_device)."""
     dev = torch.device("cuda")
     g = torch.Generator(device="cpu").manual_seed(seed)
+    gk = torch.Generator(device=dev).manual_seed(seed) if on_device else g
     L = tq.tq_get_layout(preset)
     nblk = (ctx + bs - 1) // bs
     nb = B * nblk
@@ -33,9 +36,10 @@ def _problem(seed, preset, B, Hq, Hk, bs, ctx, dtype):
     if not L["key_fp8"]:
         c, m = tq.tq_build_codebook(128, L["key_bits"])
         cent, mids = torch.from_numpy(c).to(dev), torch.from_numpy(m).to(dev)
+    kv_dev = dev if on_device else "cpu"
     for b in range(B):
-        K = torch.randn((ctx, Hk, 128), generator=g).to(dtype).to(dev)
-        V = torch.randn((ctx, Hk, 128), generator=g).to(dtype).to(dev)
+        K = torch.randn((ctx, Hk, 128), generator=gk, device=kv_dev).to(dtype).to(dev)
+        V = torch.randn((ctx, Hk, 128), generator=gk, device=kv_dev).to(dtype).to(dev)
         t = torch.arange(ctx)
         sm = (bt[b].cpu()[t // bs].long() * bs + t % bs).to(dev)
         tq.store(preset, K, V, sm, cache, bs, signs, cent, mids)
@@ -102,3 +106,23 @@ def test_no_alloc_rejects_partials_beyond_its_array():
     out = torch.empty((p["B"], p["Hq"], 128), dtype=torch.float32, device="cuda")
     lse = torch.empty((p["B"], p["Hq"]), dtype=torch.float32, device="cuda")
     assert _lib.tq_decode_attention_noalloc(*_args(p, too_many, out, lse)) == _lib.TQ_ERR_WORKSPACE
+
+
+def test_no_alloc_lowers_the_library_split_count_to_fit():
+    """With num_splits = 0 and a shape whose library-chosen split count
+    would not fit the array (B = 64 sequences x 64 query heads: about 2.1 MB
+    of partials per split, so at most 7 splits fit), the call runs with the
+    largest count that fits, and gives exactly what the workspace entry
+    point gives with that count."""
+    B, Hq, Hk = 64, 64, 8
+    per_split = tq.tq_decode_workspace_bytes(B, Hq, 1, 128)
+    fit = _lib.TQ_NOALLOC_SCRATCH_BYTES // per_split
+    ctx = next((c for c in (8192, 16384, 32768)
+                if tq.tq_decode_pick_splits(tq.TQ_K3V4_NC, 128, B, Hq, Hk, c) > fit), None)
+    assert ctx is not None, "no context length where the library picks more splits than fit"
+    p = _problem(14, tq.TQ_K3V4_NC, B=B, Hq=Hq, Hk=Hk, bs=64, ctx=ctx, dtype=torch.float16,
+                 on_device=True)
+    o1, l1 = _with_workspace(p, fit)
+    o2, l2 = _no_alloc(p, 0)
+    assert np.all(np.isfinite(o2)) and np.all(np.isfinite(l2))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
