@@ -4,14 +4,19 @@
 One step = the whole hot path on one batch: the fused store of each
 sequence's newest token (tq_store) followed by split-K decode attention over
 the packed paged cache (tq_decode_attention: stage 1 + stage 2).  Default
-workload: Llama-3-8B-shaped decode (B=32, 32 q / 8 kv heads, head_dim 128,
-8192-token contexts, block_size 16, preset turboquant_k8v4, bf16, random
-block-table permutation), synthetic seeded data.
+workload: the largest single-GPU configuration, Qwen3-32B-shaped decode
+(B=64, 64 q / 8 kv heads, head_dim 128, contexts uniform in [16K, 32K],
+block_size 64, preset turboquant_k3v4_nc, fp16, 2% Student-t(3)
+coordinates, random block-table permutation), synthetic seeded data.
 
 Prints ONE JSON line (rank 0).  `value` is packed-KV bytes read per step
 divided by the device-timed step (GB/s), summed over ranks; `e2e` is the same
 metric with every step's inputs copied from pinned host memory and the
-attention output copied back, inside the timed region.
+attention output copied back, inside the timed region.  With the default
+workload the line also carries a row per configuration (`configs`: the tiny
+case, the Llama-3-8B shape, the Qwen3-32B shape, the 256K-token case, and
+the 16K-token mixed-batch store followed by decode over its cache, every
+preset), the 1M-token store, the dequantisation and a 32K-256K context sweep.
 
 --impl reference times the CPU oracle (the slow plain-C definition of the
 method) on a bounded sample of the same workload, on the host cores.
@@ -47,7 +52,7 @@ def _args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="llama3_8b",
+    p.add_argument("--workload", default="qwen3_32b",
                    choices=["llama3_8b", "qwen3_32b", "long", "store_mixed", "sweep", "tiny"])
     p.add_argument("--preset", default=None, choices=sorted(SLOT))
     p.add_argument("--ctx", type=int, default=None)
@@ -83,52 +88,118 @@ def _kv_bytes(w) -> int:
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event (throttle) reasons of the GPU, sampled
+    every 2 ms by a thread through NVML (read-only queries, libnvidia-ml
+    through ctypes), or every 50 ms through nvidia-smi where NVML cannot be
+    loaded.  Started before the warm-up; mark() brackets the timed region."""
+    NAMES = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+             0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.rows, self.proc, self.err = [], None, None
+    def __init__(self, gpu_index: int, uuid: str | None = None):
+        self.idx, self.uuid = gpu_index, uuid
+        self.rows = []                 # (time, sm_mhz, max_mhz, power_w, reasons bitmask)
+        self.windows, self.err, self.source = [], None, None
+        self.stop = threading.Event()
+        self.proc = None
+
+    def _nvml(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = nv.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.idx), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        clk, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))       # 1 = NVML_CLOCK_SM
+
+        def sample():
+            nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))
+            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            reasons_fn(h, ctypes.byref(rs))
+            return (time.time(), float(clk.value), float(mx.value), pw.value / 1000.0, int(rs.value))
+        sample()
+        return sample
+
+    def _loop_nvml(self, sample):
+        while not self.stop.is_set():
+            self.rows.append(sample())
+            time.sleep(0.002)
+
+    def _loop_smi(self):
+        for line in self.proc.stdout:
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 7:
+                continue
+            try:
+                bits = sum(b for b, v in zip((0x8, 0x40, 0x20, 0x4), r[3:7]) if v.lower().startswith("active"))
+                self.rows.append((time.time(), float(r[0]), float(r[1]), float(r[2]), bits))
+            except ValueError:
+                pass
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except Exception as e:  # pragma: no cover
-            self.err = str(e)
+            sample = self._nvml()
+            self.source = "nvml, 2 ms"
+            self.t = threading.Thread(target=self._loop_nvml, args=(sample,), daemon=True)
+        except Exception as e:
+            self.err = f"nvml: {e}"
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                     "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi, 50 ms"
+                self.t = threading.Thread(target=self._loop_smi, daemon=True)
+            except Exception as e2:  # pragma: no cover
+                self.err += f"; nvidia-smi: {e2}"
+                return self
+        self.t.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5.0:
+            time.sleep(0.005)            # the sampler is live before the first timed step
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.rows.append([x.strip() for x in line.split(",")])
+    def mark(self, start: bool):
+        if start:
+            self.windows.append([time.time(), None])
+        elif self.windows:
+            self.windows[-1][1] = time.time()
 
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:  # pragma: no cover
                 self.proc.kill()
+        if getattr(self, "t", None):
             self.t.join(timeout=2)
 
     def summary(self):
-        if not self.rows:
+        rows = list(self.rows)
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
-                    "note": self.err or "no nvidia-smi samples"}
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4)
-                          if len(r) > 5 + i and r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.rows)}
+                    "note": self.err or "no samples"}
+        inside = [r for r in rows for a, b in self.windows if b and a <= r[0] <= b]
+        use = inside or rows
+        pmax = max(r[3] for r in use)
+        load = [r for r in use if r[3] >= 0.25 * pmax] or use
+        reasons = sorted({n for r in use for bit, n in self.NAMES.items() if r[4] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in load), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside),
+                "power_w_max": round(pmax, 1), "source": self.source,
+                "window": "samples inside the timed steps (all samples if none fell inside); "
+                          "median SM clock over those at >= 25% of their peak power"}
 
 
 def _peaks():
@@ -238,18 +309,19 @@ def _job_value(kv_bytes_per_rank: int, step_ms: float, world: int) -> float:
     return world * kv_bytes_per_rank / (step_ms * 1e-3) / 1e9
 
 
-def time_device(p: Problem, steps: int, warmup: int, world: int, gpu_index: int):
+def time_device(p: Problem, steps: int, warmup: int, world: int, gpu_index: int, gpu_uuid=None):
     import torch
     st = torch.cuda.current_stream()
-    for _ in range(warmup):
-        p.store()
-        p.decode()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    _barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(gpu_index) as clk:
+    with ClockSampler(gpu_index, gpu_uuid) as clk:
+        for _ in range(warmup):
+            p.store()
+            p.decode()
+        torch.cuda.synchronize()
+        _barrier(world)
+        torch.cuda.synchronize()
+        clk.mark(True)
         # the steps back to back: no event between the store and the decode,
         # whose stage 1 is launched as a programmatic dependent of the store
         e0.record(st)
@@ -258,6 +330,7 @@ def time_device(p: Problem, steps: int, warmup: int, world: int, gpu_index: int)
             p.decode()
         e1.record(st)
         torch.cuda.synchronize()
+        clk.mark(False)
         # the decode calls alone, back to back: the per-call duration of the
         # dominant kernels (stage 1 + stage 2) for the roofline
         e2.record(st)
@@ -269,6 +342,90 @@ def time_device(p: Problem, steps: int, warmup: int, world: int, gpu_index: int)
     total_ms = e0.elapsed_time(e1)
     dec_ms = e2.elapsed_time(e3) / steps
     return total_ms, dec_ms, clk.summary()
+
+
+def time_calls(fn, calls: int, flush_bytes: int = 0) -> float:
+    """Mean device time of fn() in ms: back to back between two events, or,
+    with flush_bytes > 0 (inputs smaller than L2), the median of single
+    calls with a buffer of that size written in between (L2 flushed)."""
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    if flush_bytes <= 0:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(st)
+        for _ in range(calls):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / calls
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda")
+    ts = []
+    for _ in range(calls):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    del flush
+    return float(np.median(ts))
+
+
+def decode_row(w, dev, peak_gbs: float, calls: int = 50) -> dict:
+    """One configuration's row: the decode call (stage 1 + stage 2) and the
+    step (store of every sequence's newest token + decode), the library's
+    split count (or the configuration's own).  Inputs larger than L2 run
+    back to back; smaller ones are timed one call at a time with L2 flushed
+    in between."""
+    import torch
+    p = Problem(w, dev, None)
+    kvb = _kv_bytes(w)
+    small = kvb <= L2_BYTES
+    flush = 256 * 2**20 if small else 0
+
+    def step():
+        p.store()
+        p.decode()
+    dec_ms = time_calls(p.decode, calls, flush)
+    step_ms = time_calls(step, calls, flush)
+    row = {"workload": _describe(w), "preset": w.preset, "batch": w.B, "q_heads": w.Hq,
+           "kv_heads": w.Hk, "block_size": w.block_size, "num_splits": p.S,
+           "kernel": "tensor-core" if _kernel_kind(p) == 1 else "CUDA-core",
+           "packed_kv_bytes": kvb, "decode_ms": round(dec_ms, 5), "step_ms": round(step_ms, 5),
+           "gbs": round(kvb / dec_ms / 1e6, 1), "frac_of_measured_hbm": round(kvb / dec_ms / 1e6 / peak_gbs, 4),
+           "decode_tok_s": round(w.B / (step_ms * 1e-3), 1),
+           "l2": "flushed between calls (inputs smaller than L2)" if small else "inputs larger than L2"}
+    del p
+    torch.cuda.empty_cache()
+    return row
+
+
+def _kernel_kind(p) -> int:
+    import quantized_kv_cache_04_gb300 as tq
+    return tq.tq_decode_kernel_kind(p.c.preset, p.w.D, p.w.Hq, p.w.Hk)
+
+
+def config_rows(dev, peak_gbs: float, headline: dict) -> dict:
+    """A row per configuration: 1 tiny, 2 Llama-3-8B shape, 3 Qwen3-32B shape
+    (the headline's own numbers), 4 the 256K-token case, 5 the mixed-batch
+    store of 16,384 tokens in one call and the decode (32 query heads) over
+    the resulting cache, every preset."""
+    rows = {"1_tiny": decode_row(wl.make("tiny"), dev, peak_gbs, 50),
+            "2_llama3_8b": decode_row(wl.make("llama3_8b"), dev, peak_gbs, 100),
+            "3_qwen3_32b": headline,
+            "4_long": decode_row(wl.make("long"), dev, peak_gbs, 30)}
+    store = time_store_mixed(dev)
+    mixed = {}
+    for preset in SLOT:
+        r = decode_row(wl.make("store_mixed", preset=preset), dev, peak_gbs, 50)
+        r["store"] = store[preset]
+        mixed[preset] = r
+    rows["5_store_mixed"] = mixed
+    return rows
 
 
 def time_e2e(p: Problem, steps: int, warmup: int, world: int):
@@ -598,12 +755,18 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     import quantized_kv_cache_04_gb300 as tq
     tq.load(build_if_missing=True)
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    if len(vis) > local and vis[local].strip().isdigit():
+        gpu_index = int(vis[local])
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # pragma: no cover
+        gpu_uuid = None
 
     p = Problem(w, dev, args.splits, args.v_threshold, args.soa)
     assert args.warmup >= 3
-    total_ms, dec_ms, clocks = time_device(p, args.steps, args.warmup, world, gpu_index)
+    total_ms, dec_ms, clocks = time_device(p, args.steps, args.warmup, world, gpu_index, gpu_uuid)
     step_ms = _max_over_ranks(total_ms / args.steps, world)
     dec_ms = _max_over_ranks(dec_ms, world)
     kvb = _kv_bytes(w)
@@ -644,13 +807,24 @@ def main():
         "decode_ms": round(dec_ms, 5),
         "output_finite": out_ok,
     }
+    default = (args.workload == "qwen3_32b" and args.preset is None and args.ctx is None
+               and args.batch is None and not args.soa and args.v_threshold == 0.0)
     if not args.no_extra and rank == 0:
-        line["store_mixed"] = time_store_mixed(dev)
-        line["store_mtok_s"] = line["store_mixed"]["turboquant_4bit_nc"]["mtok_s"]
-        line["store_1m"] = time_store_large(dev)
         line["dequant"] = time_dequant(p, peak)
-        if args.workload == "llama3_8b" and args.ctx is None and args.batch is None:
+        head = {"workload": _describe(w), "preset": w.preset, "batch": w.B, "q_heads": w.Hq,
+                "kv_heads": w.Hk, "block_size": w.block_size, "num_splits": p.S,
+                "kernel": "tensor-core" if _kernel_kind(p) == 1 else "CUDA-core",
+                "packed_kv_bytes": kvb, "decode_ms": round(dec_ms, 5), "step_ms": round(step_ms, 5),
+                "gbs": round(achieved, 1), "frac_of_measured_hbm": round(achieved / peak, 4),
+                "decode_tok_s": round(w.B / (step_ms * 1e-3), 1), "l2": "inputs larger than L2",
+                "note": "the headline run above"}
+        del p
+        torch.cuda.empty_cache()
+        if default:
+            line["configs"] = config_rows(dev, peak, head)
             line["long_context"] = time_long_context(dev, peak)
+        line["store_1m"] = time_store_large(dev)
+        line["store_mtok_s"] = {k: v["mtok_s"] for k, v in line["store_1m"].items()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:

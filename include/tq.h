@@ -298,10 +298,37 @@ int tq_decode_attention_noalloc(int preset, int head_dim, int batch, int num_q_h
                                 const int8_t* signs, const float* centroids,
                                 void* out, int out_dtype, float* lse, void* stream);
 
+/* Test entry point for the bounded waits of the tensor-core stage 1; the
+ * pages have no counterpart.  Runs tq_decode_attention (num_splits as there)
+ * with every stage wait of stage 1 limited to `wait_polls` mbarrier polls,
+ * and makes one wait run out without any fault: the tile `stuck_tile` (0 =
+ * first) of split 0 of sequence 0, kv-head group 0, is announced to its
+ * mbarrier as 16 bytes longer than the copies that fill it, so every copy
+ * lands but that stage never completes.  The warps of that CTA give up after
+ * `wait_polls` polls, wait (with the same limit) for the copies they had
+ * requested, and give the query heads of that CTA a NaN lse for split 0, so
+ * the merged output and lse of those heads of sequence 0 come out NaN; every
+ * other output is what tq_decode_attention gives.  Nothing waits without a
+ * limit, so the call returns and the context stays usable.
+ * TQ_ERR_UNSUPPORTED for shapes the CUDA-core stage 1 serves
+ * (tq_decode_kernel_kind != 1); TQ_ERR_INVALID_ARG for stuck_tile < 0 or
+ * wait_polls == 0; other errors as tq_decode_attention. */
+int tq_test_decode_wait_expiry(int preset, int head_dim, int batch, int num_q_heads,
+                               int num_kv_heads, int block_size, int q_dtype, const void* query,
+                               const uint8_t* kv_cache, long long num_blocks,
+                               const int32_t* block_table, int block_table_stride,
+                               const int32_t* seq_lens, int max_seq_len, float softmax_scale,
+                               int num_splits, const int8_t* signs, const float* centroids,
+                               void* out, int out_dtype, float* lse, void* workspace,
+                               size_t workspace_bytes, int stuck_tile, unsigned int wait_polls,
+                               void* stream);
+
 /* Which stage-1 kernel tq_decode_attention runs for this shape (host only):
- * 1 = tensor-core stage 1 (FP8 or 3-bit keys, 3/4-bit values, group size
- * <= 8, num_kv_heads <= 16, token row = num_kv_heads * slot a multiple of 16
- * bytes and at most ~1.7 KB);
+ * 1 = tensor-core stage 1: keys FP8 (k8v4), 3-bit (k3v4_nc, 3bit_nc),
+ * 4-bit with 4-bit values (4bit_nc) or 2-bit with 2-bit values (2bit_nc);
+ * group size (num_q_heads / num_kv_heads) <= 8; the bytes a CTA copies per
+ * token (all kv heads' slots, or 4 heads' for FP8 keys with num_kv_heads a
+ * multiple of 4 above 4) a multiple of 16 and at most ~1.7 KB;
  * 0 = CUDA-core stage 1 (every other supported shape); -1 = unsupported. */
 int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, int num_kv_heads);
 

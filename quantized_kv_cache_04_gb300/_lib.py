@@ -248,3 +248,17 @@ def tq_decode_attention_noalloc(*args) -> int:
                                        ctypes.c_float, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_vp,
                                        _c_vp])
     return fn(*args)
+
+
+def tq_test_decode_wait_expiry(*args) -> int:
+    """Raw C call of the wait-expiry test entry point (arguments as
+    tq_decode_attention, then stuck_tile, wait_polls, stream): one stage of
+    split 0 of sequence 0 never completes, its bounded waits run out, and
+    those heads come out NaN.  Returns the status."""
+    L = load()
+    fn = L.tq_test_decode_wait_expiry
+    if fn.argtypes is None:
+        fn.argtypes = ([_c_int] * 7 + [_c_vp, _c_vp, _c_ll, _c_vp, _c_int, _c_vp, _c_int,
+                                       ctypes.c_float, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_vp,
+                                       _c_vp, _c_sz, _c_int, ctypes.c_uint, _c_vp])
+    return fn(*args)

@@ -450,17 +450,19 @@ int pick_splits(const tq_layout& L, bool soa, int batch, int num_q_heads, int nu
 
 }  // namespace tq
 
-extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch, int num_q_heads,
-                                            int num_kv_heads, int block_size, int q_dtype,
-                                            const void* query, const uint8_t* kv_cache,
-                                            long long num_blocks, const int32_t* block_table,
-                                            int block_table_stride, const int32_t* seq_lens,
-                                            int max_seq_len, float softmax_scale, int num_splits,
-                                            const int8_t* signs, const float* centroids, void* out,
-                                            int out_dtype, float* lse, void* workspace,
-                                            size_t workspace_bytes, float v_threshold, void* stream)
+namespace tq {
+namespace {
+
+// Argument checks, split choice and the launches of both stages; stuck_tile
+// >= 0 (the wait-expiry test) needs the tensor-core stage 1.
+int decode_impl(int preset, int head_dim, int batch, int num_q_heads, int num_kv_heads, int block_size,
+                int q_dtype, const void* query, const uint8_t* kv_cache, long long num_blocks,
+                const int32_t* block_table, int block_table_stride, const int32_t* seq_lens,
+                int max_seq_len, float softmax_scale, int num_splits, const int8_t* signs,
+                const float* centroids, void* out, int out_dtype, float* lse, void* workspace,
+                size_t workspace_bytes, float v_threshold, int stuck_tile, uint32_t wait_polls,
+                void* stream)
 {
-    using namespace tq;
     tq_layout L;
     int rc = fill_layout(preset, head_dim, &L);
     if (rc) return rc;
@@ -505,10 +507,12 @@ extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch,
     a.g = geom_of(L, soa);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    if (mma_stage1_supported(L, soa, num_kv_heads, a.G)) {
+    const bool mma = mma_stage1_supported(L, soa, num_kv_heads, a.G);
+    if (stuck_tile >= 0 && !mma) return TQ_ERR_UNSUPPORTED;
+    if (mma) {
         rc = launch_mma_stage1(L, soa, q_dtype, query, kv_cache, num_blocks, block_table, block_table_stride, seq_lens,
                                softmax_scale, S, signs, centroids, a.mid, batch, num_q_heads,
-                               num_kv_heads, block_size, v_threshold, st);
+                               num_kv_heads, block_size, v_threshold, st, stuck_tile, wait_polls);
         if (rc) return rc;
     } else {
         cudaError_t e = q_dtype == TQ_F16 ? launch_stage1<__half>(preset, a, st)
@@ -519,6 +523,43 @@ extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch,
                            : out_dtype == TQ_F16 ? launch_stage2<__half>(a, st)
                                                  : launch_stage2<__nv_bfloat16>(a, st);
     return e2 == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" int tq_decode_attention_sparse_v(int preset, int head_dim, int batch, int num_q_heads,
+                                            int num_kv_heads, int block_size, int q_dtype,
+                                            const void* query, const uint8_t* kv_cache,
+                                            long long num_blocks, const int32_t* block_table,
+                                            int block_table_stride, const int32_t* seq_lens,
+                                            int max_seq_len, float softmax_scale, int num_splits,
+                                            const int8_t* signs, const float* centroids, void* out,
+                                            int out_dtype, float* lse, void* workspace,
+                                            size_t workspace_bytes, float v_threshold, void* stream)
+{
+    return tq::decode_impl(preset, head_dim, batch, num_q_heads, num_kv_heads, block_size, q_dtype, query,
+                           kv_cache, num_blocks, block_table, block_table_stride, seq_lens, max_seq_len,
+                           softmax_scale, num_splits, signs, centroids, out, out_dtype, lse, workspace,
+                           workspace_bytes, v_threshold, -1, tq::kWaitPolls, stream);
+}
+
+extern "C" int tq_test_decode_wait_expiry(int preset, int head_dim, int batch, int num_q_heads,
+                                          int num_kv_heads, int block_size, int q_dtype,
+                                          const void* query, const uint8_t* kv_cache,
+                                          long long num_blocks, const int32_t* block_table,
+                                          int block_table_stride, const int32_t* seq_lens,
+                                          int max_seq_len, float softmax_scale, int num_splits,
+                                          const int8_t* signs, const float* centroids, void* out,
+                                          int out_dtype, float* lse, void* workspace,
+                                          size_t workspace_bytes, int stuck_tile,
+                                          unsigned int wait_polls, void* stream)
+{
+    if (stuck_tile < 0 || wait_polls < 1) return TQ_ERR_INVALID_ARG;
+    return tq::decode_impl(preset, head_dim, batch, num_q_heads, num_kv_heads, block_size, q_dtype, query,
+                           kv_cache, num_blocks, block_table, block_table_stride, seq_lens, max_seq_len,
+                           softmax_scale, num_splits, signs, centroids, out, out_dtype, lse, workspace,
+                           workspace_bytes, 0.f, stuck_tile, wait_polls, stream);
 }
 
 extern "C" int tq_decode_attention(int preset, int head_dim, int batch, int num_q_heads,

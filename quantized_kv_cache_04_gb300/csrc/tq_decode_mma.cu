@@ -161,10 +161,12 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
                       long long num_blocks, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
-                      float v_threshold, cudaStream_t st)
+                      float v_threshold, cudaStream_t st, int stuck_tile, uint32_t wait_polls)
 {
     MmaArgs a;
     a.vthr = v_threshold;
+    a.stuck_tile = stuck_tile;
+    a.wait_polls = wait_polls;
     a.key_alpha = (!L.key_fp8 && L.key_bits == 2) ? two_bit_alpha() : 0.f;
     a.query = query;
     a.cache = kv_cache;

@@ -11,7 +11,7 @@ dequantised cache), and the GPU's output rows and LSEs for them must meet the
 decode tolerances.  The other sequences keep the benchmark's device-generated
 inputs.  The store configuration (16,384 new tokens of 16 sequences) is
 checked slot by slot on sampled (token, kv head) pairs against the oracle's
-store of the same inputs.
+store of the same inputs, and the decode over its cache like the others.
 """
 from __future__ import annotations
 
@@ -35,11 +35,18 @@ def _sampled(w):
     return sorted({int(order[0]), int(order[-1])})
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen3_32b", "long"])
-def test_decode_full_size_sampled(orc, name):
+DECODE_CASES = [("tiny", None), ("llama3_8b", None), ("qwen3_32b", None), ("long", None)] + [
+    ("store_mixed", p) for p in ("turboquant_k8v4", "turboquant_4bit_nc", "turboquant_k3v4_nc",
+                                 "turboquant_3bit_nc", "turboquant_2bit_nc")]
+
+
+@pytest.mark.parametrize("name,preset", DECODE_CASES)
+def test_decode_full_size_sampled(orc, name, preset):
+    """Every decode workload, and the decode (32 query heads) over the mixed
+    16-sequence cache of the store workload in every preset."""
     import bench
     dev = torch.device("cuda")
-    w = wl.make(name)
+    w = wl.make(name, preset=preset)
     p = bench.Problem(w, dev, None)
     L = orc.layout(w.preset_id)
     signs = orc.signs(128, 42)
