@@ -409,6 +409,20 @@ def _kernel_kind(p) -> int:
     return tq.tq_decode_kernel_kind(p.c.preset, p.w.D, p.w.Hq, p.w.Hk)
 
 
+def other_shape_rows(dev, peak_gbs: float) -> list:
+    """Decode at 32K contexts in shapes outside the configurations: groups of
+    16 query heads (128 q / 8 kv heads), which the CUDA-core stage 1 serves,
+    and 2 or 4 kv heads with Lloyd-Max keys (token rows that are not whole
+    16-byte units)."""
+    rows = []
+    for preset, hq, hk in (("turboquant_k8v4", 128, 8), ("turboquant_k3v4_nc", 128, 8),
+                           ("turboquant_4bit_nc", 8, 2), ("turboquant_k3v4_nc", 8, 2),
+                           ("turboquant_3bit_nc", 16, 4)):
+        w = wl.make("sweep", preset=preset, ctx=32768, q_heads=hq, kv_heads=hk)
+        rows.append(decode_row(w, dev, peak_gbs, 30))
+    return rows
+
+
 def config_rows(dev, peak_gbs: float, headline: dict) -> dict:
     """A row per configuration: 1 tiny, 2 Llama-3-8B shape, 3 Qwen3-32B shape
     (the headline's own numbers), 4 the 256K-token case, 5 the mixed-batch
@@ -823,6 +837,7 @@ def main():
         if default:
             line["configs"] = config_rows(dev, peak, head)
             line["long_context"] = time_long_context(dev, peak)
+            line["other_shapes"] = other_shape_rows(dev, peak)
         line["store_1m"] = time_store_large(dev)
         line["store_mtok_s"] = {k: v["mtok_s"] for k, v in line["store_1m"].items()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -2,6 +2,7 @@
 // dense instantiations (the kernel itself is in tq_decode_mma.cuh).
 #include "tq_decode_mma.cuh"
 
+#include <algorithm>
 #include <array>
 #include <cmath>
 
@@ -92,12 +93,15 @@ MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G)
     // warp reads in the same instruction on distinct bank quads
     m.smem_row = (m.copy_bytes % 32 == 0) ? m.copy_bytes + 16 : m.copy_bytes;
     const int stage = kTile * (m.smem_row + m.meta_bytes);
-    // ring budget: two CTAs of Hk warps, or four CTAs of 4 warps, per SM;
-    // MSE keys with G = 8 also keep 4 KB of q fragments per warp, and 3-bit
-    // keys hold their 8 KB pair table in static shared memory
+    // ring budget: two CTAs of 8 kv-head warps, or four CTAs of 4 warps, per
+    // SM (about 16 warps); fewer kv heads take a proportional share (at
+    // least 28 KB), so that CTAs of 2 or 4 warps still fill an SM.  MSE keys
+    // with G = 8 also keep 4 KB of q fragments per warp, and 3-bit keys hold
+    // their 8 KB pair table in static shared memory
     const int qsm = (!L.key_fp8 && G > 4) ? m.hpc * 4096 : 0;
     m.static_smem = (!L.key_fp8 && L.key_bits == 3) ? size_t(kLut3Entries) * 8 : 0;
-    int nst = ((m.hpc < Hk ? 56 * 1024 : 100 * 1024) + (qsm ? 12 * 1024 : 0) - qsm - int(m.static_smem)) / stage;
+    const int budget = m.hpc < Hk ? 56 * 1024 : (Hk >= 8 ? 100 * 1024 : std::max(28 * 1024, 100 * 1024 * Hk / 8));
+    int nst = (budget + (qsm ? 12 * 1024 : 0) - qsm - int(m.static_smem)) / stage;
     nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
     // the q staging at kernel start borrows the ring: hpc * (4 or 8) heads * 512 B
     while (nst * stage < m.hpc * (G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
@@ -130,7 +134,13 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
     if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > 8) return false;
     const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
     const int row = m.copy_bytes;
-    return m.hpc <= 16 && row % 16 == 0 && m.meta_bytes % 16 == 0 &&
+    // Copies are 16-byte units: rows of a multiple of 16 bytes are copied
+    // one by one (or per page segment); an AoS CTA that takes whole rows of
+    // a multiple of 4 bytes copies whole page segments (16 or 32 rows: a
+    // multiple of 16 bytes, from a 16-byte aligned page offset) into an
+    // unpadded ring.  Rows must stay 4-byte aligned for the word loads.
+    const bool rows_ok = row % 16 == 0 || (!soa && m.hpc == num_kv_heads && row % 4 == 0);
+    return m.hpc <= 16 && rows_ok && m.meta_bytes % 16 == 0 &&
            2 * kTile * (row + 16 + m.meta_bytes) <= 110 * 1024;
 }
 

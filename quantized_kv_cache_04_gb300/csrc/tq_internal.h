@@ -97,8 +97,10 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
 void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int num_sms,
                       int* ctas_per_split, int* slots);
 // Polls of a stage's mbarrier before stage 1 gives up on it (the split's
-// lse becomes NaN); a test may pass a small count and a stuck tile.
-constexpr uint32_t kWaitPolls = 1u << 24;
+// lse becomes NaN); each poll sleeps at most 20 us waiting for the phase,
+// so a stage that never completes is given up after about 1.3 s.  A test
+// may pass a small count and a stuck tile.
+constexpr uint32_t kWaitPolls = 1u << 16;
 int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* query, const uint8_t* kv_cache,
                       long long num_blocks, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,

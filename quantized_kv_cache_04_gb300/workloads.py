@@ -79,7 +79,8 @@ def _paging(seq_lens: np.ndarray, bs: int, rng: np.random.Generator, shuffle: bo
 
 
 def make(name: str, preset: str | None = None, seed: int | None = None,
-         batch: int | None = None, ctx: int | None = None) -> Workload:
+         batch: int | None = None, ctx: int | None = None,
+         q_heads: int | None = None, kv_heads: int | None = None) -> Workload:
     """Build the paging metadata and value recipe of a named workload.
 
     tiny        B=1, Hq=8, Hk=2, ctx 512, bs 16, 4bit_nc, fp16, 4 outlier channels x8
@@ -91,7 +92,8 @@ def make(name: str, preset: str | None = None, seed: int | None = None,
                 high-similarity key every 4096 tokens, 64 splits
     store_mixed 16 sequences, geometric lengths (mean 1024) rescaled to 16384
                 tokens, bs 32, Hk 8, Hq 32, fp16, any preset (default 4bit_nc)
-    sweep       like llama3_8b at a given context (B*ctx ~ 1M tokens), any preset
+    sweep       like llama3_8b at a given context (B*ctx ~ 1M tokens), any preset;
+                q_heads / kv_heads change its head counts (e.g. groups of 16)
     """
     base_seed = {"tiny": 1001, "llama3_8b": 1002, "qwen3_32b": 1003, "long": 1004,
                  "store_mixed": 1005, "sweep": 1006}[name]
@@ -112,6 +114,7 @@ def make(name: str, preset: str | None = None, seed: int | None = None,
         if name == "sweep":
             L = ctx or 32768
             B = max(1, (1 << 20) // L)
+            Hq, Hk = q_heads or Hq, kv_heads or Hk
         elif ctx is not None:
             L = ctx
         if batch is not None:

@@ -48,19 +48,23 @@ CASES = [  # (G, Hk, bs, seq_lens, splits): CUDA-core and tensor-core stage 1 sh
     (6, 8, 16, [250, 0], 5),
     (5, 16, 32, [90, 333], 0),
     (16, 8, 16, [200], 2),
+    (2, 1, 32, [300, 45], 0),
+    (4, 3, 16, [77, 400], 0),
 ]
 
 
 def _expected_kind(preset, G, Hk):
     """Tensor-core stage 1 serves every preset with G <= 8.  A CTA takes the
     token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above 4) or of all
-    Hk <= 16 heads; that part of a row must be whole 16-byte units and a
-    two-stage ring of 32 such rows must fit in ~110 KB of shared memory."""
+    Hk <= 16 heads; that part of a row must be whole 16-byte units, or, when
+    the CTA takes whole rows, a multiple of 4 bytes (copied per page
+    segment); and a two-stage ring of 32 such rows must fit in ~110 KB of
+    shared memory."""
     slot = [196, 134, 118, 102, 70][preset]
     hpc = 4 if (preset == 0 and Hk % 4 == 0 and Hk > 4) else Hk
     row = hpc * slot
-    return int(G <= 8 and hpc <= 16 and row % 16 == 0
-               and 2 * 32 * (row + 16) <= 110 * 1024)
+    rows_ok = row % 16 == 0 or (hpc == Hk and row % 4 == 0)
+    return int(G <= 8 and hpc <= 16 and rows_ok and 2 * 32 * (row + 16) <= 110 * 1024)
 
 
 @pytest.mark.parametrize("preset", PRESETS)
