@@ -411,9 +411,9 @@ def _kernel_kind(p) -> int:
 
 def other_shape_rows(dev, peak_gbs: float) -> list:
     """Decode at 32K contexts in shapes outside the configurations: groups of
-    16 query heads (128 q / 8 kv heads), which the CUDA-core stage 1 serves,
-    and 2 or 4 kv heads with Lloyd-Max keys (token rows that are not whole
-    16-byte units)."""
+    16 query heads (128 q / 8 kv heads: two CTAs of 8 query heads per kv
+    head), and 2 or 4 kv heads with Lloyd-Max keys (token rows that are not
+    whole 16-byte units)."""
     rows = []
     for preset, hq, hk in (("turboquant_k8v4", 128, 8), ("turboquant_k3v4_nc", 128, 8),
                            ("turboquant_4bit_nc", 8, 2), ("turboquant_k3v4_nc", 8, 2),

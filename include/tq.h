@@ -326,9 +326,11 @@ int tq_test_decode_wait_expiry(int preset, int head_dim, int batch, int num_q_he
 /* Which stage-1 kernel tq_decode_attention runs for this shape (host only):
  * 1 = tensor-core stage 1: keys FP8 (k8v4), 3-bit (k3v4_nc, 3bit_nc),
  * 4-bit with 4-bit values (4bit_nc) or 2-bit with 2-bit values (2bit_nc);
- * group size (num_q_heads / num_kv_heads) <= 8; the bytes a CTA copies per
- * token (all kv heads' slots, or 4 heads' for FP8 keys with num_kv_heads a
- * multiple of 4 above 4) a multiple of 16 and at most ~1.7 KB;
+ * group size (num_q_heads / num_kv_heads) <= 16 (a CTA takes up to 8 query
+ * heads of each kv head); the bytes a CTA copies per token (all kv heads'
+ * slots, or 4 heads' for FP8 keys with num_kv_heads a multiple of 4 above
+ * 4) a multiple of 16, or a multiple of 4 when they are whole token rows,
+ * and at most ~1.7 KB;
  * 0 = CUDA-core stage 1 (every other supported shape); -1 = unsupported. */
 int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, int num_kv_heads);
 

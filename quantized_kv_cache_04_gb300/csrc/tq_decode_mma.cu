@@ -131,7 +131,7 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
                          (!L.key_fp8 && (L.key_bits == 3 || (L.key_bits == 4 && L.value_bits == 4) ||
                                          (L.key_bits == 2 && L.value_bits == 2)));
     const bool vals_ok = L.value_bits >= 2 && L.value_bits <= 4;
-    if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > 8) return false;
+    if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > kMaxGroup) return false;
     const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
     const int row = m.copy_bytes;
     // Copies are 16-byte units: rows of a multiple of 16 bytes are copied
@@ -148,7 +148,7 @@ void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group,
                       int* ctas_per_split, int* slots)
 {
     const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
-    *ctas_per_split = num_kv_heads / m.hpc;
+    *ctas_per_split = num_kv_heads / m.hpc * (group > 4 ? (group + 7) / 8 : 1);
     int n = 0;
     if (num_sms > 0) {
         if (L.key_fp8) n = group <= 4 ? slots_t<8, 4, 4>(m, soa, num_sms) : slots_t<8, 4, 8>(m, soa, num_sms);
@@ -197,6 +197,9 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
     a.row_bytes = Hk * L.slot_size_aligned;
     const MmaGeom m = mma_geom(L, soa, Hk, a.G);
     a.hpc = m.hpc;
+    // groups above 8: CTAs of 8 query heads per kv head, each reading the
+    // kv heads' rows (neighbouring CTAs: the second read mostly hits L2)
+    a.nqg = a.G > 4 ? (a.G + 7) / 8 : 1;
     a.copy_bytes = m.copy_bytes;
     a.smem_row = m.smem_row;
     a.meta_bytes = m.meta_bytes;

@@ -57,6 +57,7 @@ struct MmaArgs {
     int Hq, Hk, G, bs, bs_log2;
     int row_bytes;           // global token row: Hk * slot
     int hpc;                 // kv heads per CTA (Hk, or 4 for FP8 keys)
+    int nqg;                 // query-head groups per kv head: CTAs of up to 8 of its G query heads
     int copy_bytes;          // AoS: hpc * slot; SoA: hpc * data record (the data part a CTA copies)
     int smem_row;            // copy_bytes padded to 16 mod 32 bytes
     int meta_bytes;          // SoA: hpc * metadata record per token (0 for AoS)
@@ -633,14 +634,19 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // stream (typically the store of the step's new tokens): wait for it to
     // complete before the first read of global memory
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int split = blockIdx.x;
+    const int qg = blockIdx.x % a.nqg;        // which 8 query heads of each kv head (G > 8)
+    const int split = blockIdx.x / a.nqg;
     const int b = a.lpt ? seq_of_rank(a.seq_lens, gridDim.y, blockIdx.y, reinterpret_cast<int*>(smem))
                         : blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int h0 = blockIdx.z * a.hpc;        // first kv head of this CTA
     const int h = h0 + warp;                   // this warp's kv head
-    const int S = a.num_splits, Hq = a.Hq, Greal = a.G;
+    // query heads of this CTA per kv head: Greal of them from qh0 (all G
+    // when G <= 8); query head of (kv head hh, column g) = hh * Gall + qh0 + g
+    const int S = a.num_splits, Hq = a.Hq, Gall = a.G;
+    const int qh0 = 8 * qg;
+    const int Greal = a.nqg > 1 ? min(8, Gall - qh0) : Gall;
     const int Hc = a.hpc;
     const int nwarps = blockDim.x >> 5;
 
@@ -655,7 +661,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         // block to read them from: a NaN lse
         const float lse0 = t_begin >= t_end ? -INFINITY : __int_as_float(0x7fc00000);
         for (int i = threadIdx.x; i < Hc * Greal * (kHeadDim + 1); i += blockDim.x) {
-            const int hq = h0 * Greal + i / (kHeadDim + 1), d = i % (kHeadDim + 1);
+            const int r = i / (kHeadDim + 1), d = i % (kHeadDim + 1);
+            const int hq = (h0 + r / Greal) * Gall + qh0 + r % Greal;
             float* m = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
             m[d] = d == kHeadDim ? lse0 : 0.f;
         }
@@ -719,7 +726,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             fence_async_shared();             // prior generic reads of this stage before the async writes
             // the test hook's tile expects 16 bytes that no copy brings: its
             // stage never completes and the bounded waits run out
-            const uint32_t extra = (tile == a.stuck_tile && split == 0 && b == 0 && blockIdx.z == 0) ? 16u : 0u;
+            const uint32_t extra =
+                (tile == a.stuck_tile && split == 0 && qg == 0 && b == 0 && blockIdx.z == 0) ? 16u : 0u;
             mbar_expect_tx(bar, uint32_t(nd * len_d * cb + nm * len_m * mb) + extra);
         }
         __syncwarp();
@@ -815,7 +823,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         for (int g = 0; g < G; ++g) {
             float qv[4] = {0.f, 0.f, 0.f, 0.f};
             if (g < Greal) {        // warp-uniform
-                const TQ* qp = Q + ((long long)b * Hq + h * Greal + g) * kHeadDim + 4 * lane;
+                const TQ* qp = Q + ((long long)b * Hq + h * Gall + qh0 + g) * kHeadDim + 4 * lane;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) qv[i] = sgn[i] * to_f32(qp[i]);
                 if constexpr (KMODE != 8) {
@@ -1136,8 +1144,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         __syncwarp();
         if (last && *reinterpret_cast<volatile int*>(bad_pages))
             for (int i = lane; i < Hc * Greal; i += 32)
-                a.mid[(((long long)b * Hq + h0 * Greal + i) * S + split) * (kHeadDim + 1) + kHeadDim] =
-                    __int_as_float(0x7fc00000);
+                a.mid[(((long long)b * Hq + (h0 + i / Greal) * Gall + qh0 + i % Greal) * S + split) *
+                          (kHeadDim + 1) + kHeadDim] = __int_as_float(0x7fc00000);
     };
     if (failed_at >= 0) {
         // let the copies that may still be in flight (tiles failed_at ..
@@ -1146,7 +1154,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         for (int it = failed_at; it < min(ntiles, failed_at + NST); ++it)
             mbar_wait(&full[it % NST], uint32_t((it / NST) & 1), a.wait_polls);
         if (lane < Greal)
-            a.mid[(((long long)b * Hq + h * Greal + lane) * S + split) * (kHeadDim + 1) + kHeadDim] =
+            a.mid[(((long long)b * Hq + h * Gall + qh0 + lane) * S + split) * (kHeadDim + 1) + kHeadDim] =
                 __int_as_float(0x7fc00000);
         finish();
         return;
@@ -1166,7 +1174,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     for (int j = 0; j < NH; ++j) {
         const int g = G == 4 ? tig : 2 * tig + j;
         if (g >= Greal) continue;
-        const int hq = h * Greal + g;
+        const int hq = h * Gall + qh0 + g;
         float* mp = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
         const float inv = 1.f / l_run[j];
 #pragma unroll
@@ -1191,7 +1199,7 @@ cudaError_t launch_t(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_splits, B, a.Hk / a.hpc);
+    cfg.gridDim = dim3(a.num_splits * a.nqg, B, a.Hk / a.hpc);   // a split's query-head groups side by side
     cfg.blockDim = dim3(32 * a.hpc);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;

@@ -54,12 +54,12 @@ def test_out_of_range_pages_give_nan_rows(orc, preset, G, Hk, bs, splits):
     cache = big[1:nb + 1]                      # num_blocks = nb
     assert cache.shape[0] == nb and cache.is_contiguous()
     q = torch.from_numpy(rng.normal(size=(len(seq_lens), G * Hk, 128))).to(torch.float16)
-    # the CUDA-core stage 1 serves G = 16, and Hk = 1 with Lloyd-Max keys
-    # (a 134/118/102/70-byte row is not 4-byte aligned); the tensor-core one
-    # the rest (rows of 4 or 8 heads' slots, or whole rows of a multiple of 4)
+    # the CUDA-core stage 1 serves Hk = 1 with Lloyd-Max keys (a
+    # 134/118/102/70-byte row is not 4-byte aligned); the tensor-core one the
+    # rest (rows of 4 or 8 heads' slots, or whole rows of a multiple of 4)
     kind = tq.tq_decode_kernel_kind(preset, 128, G * Hk, Hk)
     slot = [196, 134, 118, 102, 70][preset]
-    assert kind == (1 if G <= 8 and (Hk * slot) % 4 == 0 else 0)
+    assert kind == (1 if (Hk * slot) % 4 == 0 else 0)
 
     ref_o, ref_l = _decode(preset, q, cache, bt, seq_lens, Hk, bs, pb["signs"], pb["c32"], splits)
     assert np.all(np.isfinite(ref_o)) and np.all(np.isfinite(ref_l))

@@ -54,7 +54,8 @@ CASES = [  # (G, Hk, bs, seq_lens, splits): CUDA-core and tensor-core stage 1 sh
 
 
 def _expected_kind(preset, G, Hk):
-    """Tensor-core stage 1 serves every preset with G <= 8.  A CTA takes the
+    """Tensor-core stage 1 serves every preset with G <= 16 (CTAs of up to 8
+    query heads per kv head).  A CTA takes the
     token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above 4) or of all
     Hk <= 16 heads; that part of a row must be whole 16-byte units, or, when
     the CTA takes whole rows, a multiple of 4 bytes (copied per page
@@ -64,7 +65,7 @@ def _expected_kind(preset, G, Hk):
     hpc = 4 if (preset == 0 and Hk % 4 == 0 and Hk > 4) else Hk
     row = hpc * slot
     rows_ok = row % 16 == 0 or (hpc == Hk and row % 4 == 0)
-    return int(G <= 8 and hpc <= 16 and rows_ok and 2 * 32 * (row + 16) <= 110 * 1024)
+    return int(G <= 16 and hpc <= 16 and rows_ok and 2 * 32 * (row + 16) <= 110 * 1024)
 
 
 @pytest.mark.parametrize("preset", PRESETS)

@@ -76,8 +76,8 @@ def test_bounded_wait_runs_out_and_marks_the_split(preset):
 
 def test_wait_expiry_rejects_the_cuda_core_path():
     import bench
-    # groups of 16 query heads: the CUDA-core stage 1
-    w = wl.make("sweep", preset="turboquant_k3v4_nc", ctx=512, batch=1, q_heads=32, kv_heads=2)
+    # one kv head with 3-bit keys: 118-byte token rows, the CUDA-core stage 1
+    w = wl.make("sweep", preset="turboquant_k3v4_nc", ctx=512, batch=1, q_heads=4, kv_heads=1)
     p = bench.Problem(w, torch.device("cuda"), 4)
     assert tq.tq_decode_kernel_kind(p.c.preset, 128, w.Hq, w.Hk) == 0
     out = torch.empty((w.B, w.Hq, 128), dtype=torch.float32, device="cuda")
