@@ -259,6 +259,251 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// The AoS store with two kv heads per warp (even kv-head counts): half-warp
+// hw = lane >> 4 takes head 2 * warp + hw, lane l = lane & 15 its dims
+// 8l .. 8l + 7.  Against a warp per head this halves the reductions' and the
+// scalar steps' instructions per head (one instruction serves both halves)
+// and takes the transform in 3 local and 4 shuffle stages instead of 2 and 5.
+
+// Sum / min / max over the 16 lanes of a half-warp.
+__device__ __forceinline__ float half_sum(float v)
+{
+#pragma unroll
+    for (int m = 8; m; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+__device__ __forceinline__ float half_min(float v)
+{
+#pragma unroll
+    for (int m = 8; m; m >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+__device__ __forceinline__ float half_max(float v)
+{
+#pragma unroll
+    for (int m = 8; m; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+// Unnormalised Sylvester Walsh-Hadamard transform of a 128-vector held 8
+// consecutive elements per lane of a half-warp (element 8l + i is v[i]):
+// index bits 0-2 inside the lane, bits 3-6 across lanes.  Each butterfly
+// maps (x_lo, x_hi) -> (x_lo + x_hi, x_lo - x_hi); across lanes the upper
+// partner computes fma(x, -1, p) = p - x and the lower fma(x, 1, p) = x + p.
+__device__ __forceinline__ void fwht128_half(float (&v)[8], int l)
+{
+#pragma unroll
+    for (int b = 1; b < 8; b <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (!(i & b)) {
+                const float x = v[i], y = v[i + b];
+                v[i] = x + y;
+                v[i + b] = x - y;
+            }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+        const float sg = (l & m) ? -1.f : 1.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float p = __shfl_xor_sync(0xffffffffu, v[i], m);
+            v[i] = __fmaf_rn(v[i], sg, p);
+        }
+    }
+}
+
+// The 8 input elements of lane l of half-warp head h for token n: 16-byte
+// loads when rows are 16-byte aligned (vec 2), 8-byte (vec 1), else 2-byte.
+template <typename T>
+__device__ __forceinline__ uint4 load8(const T* base, long long stride, int n, int h, int l, int vec)
+{
+    const T* p = base + n * stride + (long long)h * kHeadDim + 8 * l;
+    if (vec == 2) return *reinterpret_cast<const uint4*>(p);
+    if (vec == 1) {
+        const uint2 a = reinterpret_cast<const uint2*>(p)[0], b = reinterpret_cast<const uint2*>(p)[1];
+        return make_uint4(a.x, a.y, b.x, b.y);
+    }
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+    return make_uint4(uint32_t(q[0]) | uint32_t(q[1]) << 16, uint32_t(q[2]) | uint32_t(q[3]) << 16,
+                      uint32_t(q[4]) | uint32_t(q[5]) << 16, uint32_t(q[6]) | uint32_t(q[7]) << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack8(uint4 r, float (&x)[8])
+{
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint16_t u = uint16_t(w[i >> 1] >> (16 * (i & 1)));
+        if constexpr (std::is_same<T, __half>::value) x[i] = __half2float(__ushort_as_half(u));
+        else x[i] = __bfloat162float(__ushort_as_bfloat16(u));
+    }
+}
+
+// The 8 codes of lane l (code 8l + i = c[i]) as a BITS-wide LSB-first
+// bitstream at dst (2-byte aligned); all 16 lanes of the half take part.
+template <int BITS>
+__device__ __forceinline__ void pack8(uint8_t* dst, const int (&c)[8], int l)
+{
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= uint32_t(c[i]) << (BITS * i);
+    uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+    if constexpr (BITS == 4) {
+        d16[2 * l] = uint16_t(w);
+        d16[2 * l + 1] = uint16_t(w >> 16);
+    } else if constexpr (BITS == 2) {
+        d16[l] = uint16_t(w);
+    } else {
+        // lanes 2m, 2m + 1: 48 bits = three aligned 16-bit words at word 3m
+        static_assert(BITS == 3, "2, 3 or 4 bits");
+        const uint32_t nxt = __shfl_down_sync(0xffffffffu, w, 1);
+        if (!(l & 1)) {
+            d16[3 * (l >> 1)] = uint16_t(w);
+            d16[3 * (l >> 1) + 1] = uint16_t((w >> 16) | (nxt << 8));
+        } else {
+            d16[3 * (l >> 1) + 2] = uint16_t(w >> 8);
+        }
+    }
+}
+
+template <typename T, bool KEY_FP8, int KBITS, int VBITS, bool NORM_CORR>
+__global__ void __launch_bounds__(512) store2_kernel(StoreArgs a)
+{
+    __shared__ float s_cent[16], s_mid[16];
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31, hw = lane >> 4, l = lane & 15;
+    const int h = 2 * (threadIdx.x >> 5) + hw;
+    const int S = a.g.slot;
+    const int row_bytes = a.num_kv_heads * S;
+
+    if constexpr (!KEY_FP8) {
+        constexpr int NC = 1 << KBITS;
+        if (threadIdx.x < NC) s_cent[threadIdx.x] = a.centroids[threadIdx.x];
+        if (threadIdx.x < NC - 1) s_mid[threadIdx.x] = a.midpoints[threadIdx.x];
+    }
+    float sgn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sgn[i] = float(a.signs[8 * l + i]);
+    __syncthreads();
+
+    const T* K = static_cast<const T*>(a.key);
+    const T* V = static_cast<const T*>(a.value);
+    const int vec = a.vec;
+
+    // the inputs and slots of the next two tokens are in flight while this
+    // one is encoded
+    int n = blockIdx.x;
+    uint4 kr[2], vr[2];
+    long long sl[2] = {-1, -1};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int m = n + u * gridDim.x;
+        kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (m < a.num_tokens) {
+            kr[u] = load8(K, a.key_stride, m, h, l, vec);
+            vr[u] = load8(V, a.value_stride, m, h, l, vec);
+            sl[u] = a.slot_mapping[m];
+        }
+    }
+    for (; n < a.num_tokens; n += gridDim.x) {
+        const long long slot_idx = sl[0];
+        float k[8], v[8];
+        unpack8<T>(kr[0], k);
+        unpack8<T>(vr[0], v);
+        kr[0] = kr[1];
+        vr[0] = vr[1];
+        sl[0] = sl[1];
+        const int nn = n + 2 * gridDim.x;
+        if (nn < a.num_tokens) {
+            kr[1] = load8(K, a.key_stride, nn, h, l, vec);
+            vr[1] = load8(V, a.value_stride, nn, h, l, vec);
+            sl[1] = a.slot_mapping[nn];
+        }
+        if (slot_idx < 0 || slot_idx >= a.num_slots) continue;   // uniform across the CTA
+        uint8_t* dst = a.cache + slot_idx * (long long)row_bytes + h * S;
+
+        // ---------------- keys
+        if constexpr (KEY_FP8) {
+            uint32_t b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) b[i] = __nv_cvt_float_to_fp8(k[i], __NV_SATFINITE, __NV_E4M3);
+            uint16_t* d16 = reinterpret_cast<uint16_t*>(dst + 8 * l);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d16[i] = uint16_t(b[2 * i] | (b[2 * i + 1] << 8));
+        } else {
+            float n2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) n2 = __fmaf_rn(k[i], k[i], n2);
+            n2 = half_sum(n2);
+            const float nrm = __fsqrt_rn(n2);
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = sgn[i] * k[i];
+            fwht128_half(x, l);
+            // y = H(s.k)/||k|| with H = Sylvester / sqrt(128)
+            const float inv = nrm > 0.f ? __fdiv_rn(0.08838834764831845f, nrm) : 0.f;
+            int idx[8];
+            float cn = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float y = x[i] * inv;
+                int j = 0;
+#pragma unroll
+                for (int step = 1 << (KBITS - 1); step; step >>= 1)
+                    if (y > s_mid[j + step - 1]) j += step;
+                idx[i] = j;
+                const float c = s_cent[j];
+                cn = __fmaf_rn(c, c, cn);
+            }
+            cn = half_sum(cn);
+            const float stored = NORM_CORR ? __fdiv_rn(nrm, __fsqrt_rn(cn)) : nrm;
+            pack8<KBITS>(dst, idx, l);
+            if (l == 0) put_u16(dst + a.g.off_k_norm, __half_as_ushort(__float2half_rn(stored)));
+        }
+
+        // ---------------- values: asymmetric min/max uniform codes
+        {
+            constexpr int QMAX = (1 << VBITS) - 1;
+            float lo = v[0], hi = v[0];
+#pragma unroll
+            for (int i = 1; i < 8; ++i) { lo = fminf(lo, v[i]); hi = fmaxf(hi, v[i]); }
+            lo = half_min(lo);
+            hi = half_max(hi);
+            const __half scale16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), float(QMAX)));
+            const __half zero16 = __float2half_rn(lo);
+            const float sc = __half2float(scale16), z = __half2float(zero16);
+            // code = rint((v - z) / sc) with the division correctly rounded.
+            // m = fma(t, fl(1/sc), 1.5 * 2^23) rounds the exact product
+            // t * fl(1/sc) to an integer r (half to even), which is its bits
+            // minus those of 1.5 * 2^23.  For quotients below 16 that product
+            // is within 2^-19 of the correctly rounded quotient, so both
+            // round alike unless d = t * fl(1/sc) - r is within 2^-16 of
+            // +-1/2, where the exact division decides; larger quotients clamp
+            // to QMAX either way.  sc = 0 gives fl(1/sc) := 0 and code 0.
+            const float rsc = sc > 0.f ? __frcp_rn(sc) : 0.f;
+            int code[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float t = __fsub_rn(v[i], z);
+                const float m = __fmaf_rn(t, rsc, 12582912.f);
+                const float r = __fsub_rn(m, 12582912.f);
+                const float d = __fmaf_rn(t, rsc, -r);
+                int c = __float_as_int(m) - 0x4B400000;
+                if (fabsf(d) > 0.5f - 0x1p-16f) c = int(rintf(__fdiv_rn(t, sc)));
+                code[i] = min(max(c, 0), QMAX);
+            }
+            pack8<VBITS>(dst + a.g.off_v_data, code, l);
+            if (l == 0) {
+                put_u16(dst + a.g.off_v_scale, __half_as_ushort(scale16));
+                put_u16(dst + a.g.off_v_zero, __half_as_ushort(zero16));
+                if (a.slot_size < S) dst[S - 1] = 0;
+            }
+        }
+    }
+}
+
 // Grid of the grid-stride store: every CTA takes the same number of tokens,
 // so the grid is the CTAs that fit on the device at once (one wave; a second
 // partial wave would finish last with a whole share each).  Resident CTAs
@@ -267,14 +512,18 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
 template <typename T, bool KEY_FP8, int KBITS, int VBITS, bool NORM_CORR>
 cudaError_t launch_one(const StoreArgs& a, cudaStream_t st)
 {
-    auto kernel = store_kernel<T, KEY_FP8, KBITS, VBITS, NORM_CORR>;
-    static std::atomic<int> cache[16][33];     // devices x kv heads: resident CTAs on the device
-    const int threads = 32 * a.num_kv_heads;
-    const size_t smem = size_t(a.num_kv_heads) * a.g.slot;
+    // two kv heads per warp for AoS caches with an even kv-head count; a
+    // warp per head otherwise (SoA stages the token's slots in shared memory)
+    const bool pairs = !a.g.soa && a.num_kv_heads % 2 == 0;
+    auto kernel = pairs ? store2_kernel<T, KEY_FP8, KBITS, VBITS, NORM_CORR>
+                        : store_kernel<T, KEY_FP8, KBITS, VBITS, NORM_CORR>;
+    static std::atomic<int> cache[2][16][33];  // kernel x devices x kv heads: resident CTAs on the device
+    const int threads = pairs ? 16 * a.num_kv_heads : 32 * a.num_kv_heads;
+    const size_t smem = pairs ? 0 : size_t(a.num_kv_heads) * a.g.slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); dev = 0; }
     const bool keep = dev >= 0 && dev < 16;
-    int n = keep ? cache[dev][a.num_kv_heads].load(std::memory_order_relaxed) : 0;
+    int n = keep ? cache[pairs][dev][a.num_kv_heads].load(std::memory_order_relaxed) : 0;
     if (n <= 0) {
         int sms = 0, per_sm = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = kNumSMs;
@@ -282,7 +531,7 @@ cudaError_t launch_one(const StoreArgs& a, cudaStream_t st)
             per_sm = 4;
         cudaGetLastError();
         n = sms * per_sm;
-        if (keep) cache[dev][a.num_kv_heads].store(n, std::memory_order_relaxed);
+        if (keep) cache[pairs][dev][a.num_kv_heads].store(n, std::memory_order_relaxed);
     }
     kernel<<<a.num_tokens < n ? a.num_tokens : n, threads, smem, st>>>(a);
     return cudaGetLastError();
@@ -345,8 +594,11 @@ extern "C" int tq_store(int preset, int head_dim, int num_tokens, int num_kv_hea
     a.g = geom_of(L, is_soa(preset));
     // 8-byte input loads need 8-byte aligned rows: both bases, and strides of
     // a multiple of 4 elements
-    a.vec = ((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value)) & 7) == 0 &&
-            key_stride_tok % 4 == 0 && value_stride_tok % 4 == 0;
+    // (the two-heads-per-warp kernel takes 16-byte loads when the rows are
+    // 16-byte aligned: vec = 2)
+    const uintptr_t base = reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value);
+    a.vec = (base & 7) == 0 && key_stride_tok % 4 == 0 && value_stride_tok % 4 == 0;
+    if (a.vec && (base & 15) == 0 && key_stride_tok % 8 == 0 && value_stride_tok % 8 == 0) a.vec = 2;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = in_dtype == TQ_F16 ? launch_store_t<__half>(preset, a, st)
                                        : launch_store_t<__nv_bfloat16>(preset, a, st);
