@@ -437,13 +437,16 @@ __global__ void __launch_bounds__(512) store2_kernel(StoreArgs a)
 #pragma unroll
             for (int i = 0; i < 8; ++i) n2 = __fmaf_rn(k[i], k[i], n2);
             n2 = half_sum(n2);
-            const float nrm = __fsqrt_rn(n2);
             float x[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = sgn[i] * k[i];
             fwht128_half(x, l);
-            // y = H(s.k)/||k|| with H = Sylvester / sqrt(128)
-            const float inv = nrm > 0.f ? __fdiv_rn(0.08838834764831845f, nrm) : 0.f;
+            // y = H(s.k)/||k|| with H = Sylvester / sqrt(128).  The scales
+            // use rsqrtf (within 2 ulp): a relative error of ~2^-22 moves y
+            // far less than the 1e-5 a code may flip within, and the stored
+            // norm far less than its fp16 ulp
+            const float rn = n2 > 0.f ? rsqrtf(n2) : 0.f;
+            const float inv = 0.08838834764831845f * rn;
             int idx[8];
             float cn = 0.f;
 #pragma unroll
@@ -451,14 +454,14 @@ __global__ void __launch_bounds__(512) store2_kernel(StoreArgs a)
                 const float y = x[i] * inv;
                 int j = 0;
 #pragma unroll
-                for (int step = 1 << (KBITS - 1); step; step >>= 1)
-                    if (y > s_mid[j + step - 1]) j += step;
+                for (int step = 1 << (KBITS - 1); step; step >>= 1) j = y > s_mid[j + step - 1] ? j + step : j;
                 idx[i] = j;
                 const float c = s_cent[j];
                 cn = __fmaf_rn(c, c, cn);
             }
             cn = half_sum(cn);
-            const float stored = NORM_CORR ? __fdiv_rn(nrm, __fsqrt_rn(cn)) : nrm;
+            // ||k|| / ||c[idx]|| = n2 * rsqrt(n2) * rsqrt(cn)
+            const float stored = NORM_CORR ? n2 * rn * rsqrtf(cn) : n2 * rn;
             pack8<KBITS>(dst, idx, l);
             if (l == 0) put_u16(dst + a.g.off_k_norm, __half_as_ushort(__float2half_rn(stored)));
         }
@@ -484,16 +487,26 @@ __global__ void __launch_bounds__(512) store2_kernel(StoreArgs a)
             // to QMAX either way.  sc = 0 gives fl(1/sc) := 0 and code 0.
             const float rsc = sc > 0.f ? __frcp_rn(sc) : 0.f;
             int code[8];
+            bool near[8], any_near = false;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float t = __fsub_rn(v[i], z);
                 const float m = __fmaf_rn(t, rsc, 12582912.f);
                 const float r = __fsub_rn(m, 12582912.f);
                 const float d = __fmaf_rn(t, rsc, -r);
-                int c = __float_as_int(m) - 0x4B400000;
-                if (fabsf(d) > 0.5f - 0x1p-16f) c = int(rintf(__fdiv_rn(t, sc)));
-                code[i] = min(max(c, 0), QMAX);
+                code[i] = __float_as_int(m) - 0x4B400000;
+                near[i] = fabsf(d) > 0.5f - 0x1p-16f;
+                any_near |= near[i];
             }
+            // near a half-integer (rare): the exact quotient decides; one
+            // warp-uniform test instead of a branch per code
+            if (__any_sync(0xffffffffu, any_near)) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (near[i]) code[i] = int(rintf(__fdiv_rn(__fsub_rn(v[i], z), sc)));
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) code[i] = min(max(code[i], 0), QMAX);
             pack8<VBITS>(dst + a.g.off_v_data, code, l);
             if (l == 0) {
                 put_u16(dst + a.g.off_v_scale, __half_as_ushort(scale16));
