@@ -53,7 +53,8 @@ def _args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="qwen3_32b",
-                   choices=["llama3_8b", "qwen3_32b", "long", "store_mixed", "sweep", "tiny"])
+                   choices=["llama3_8b", "qwen3_32b", "long", "store_mixed", "sweep", "tiny", "store_large"],
+                   help="store_large: only the 2^20-token store of --preset (default k3v4_nc)")
     p.add_argument("--preset", default=None, choices=sorted(SLOT))
     p.add_argument("--ctx", type=int, default=None)
     p.add_argument("--batch", type=int, default=None)
@@ -534,14 +535,14 @@ def time_store_mixed(dev):
     return res
 
 
-def time_store_large(dev, tokens: int = 1 << 20):
+def time_store_large(dev, tokens: int = 1 << 20, presets=tuple(SLOT)):
     """Store throughput at scale: 2^20 tokens (16 sequences of 64K, the
     Llama-3-8B shape: 8 kv heads, bs 16, bf16) in one call, every preset;
     median of 10 calls, L2 flushed between them."""
     import torch
     import quantized_kv_cache_04_gb300 as tq
     res = {}
-    for preset in SLOT:
+    for preset in presets:
         w = wl.make("sweep", ctx=tokens // 16, preset=preset)
         ks, vs, sms = [], [], []
         for b in range(w.B):
@@ -753,9 +754,28 @@ def run_reference(args, w, rank, world):
                 "d2h_bytes_per_step": 0}}), flush=True)
 
 
+def run_store_large(args, rank):
+    """Only the 2^20-token store of one preset (for profiling the store)."""
+    import torch
+    import quantized_kv_cache_04_gb300 as tq
+    if args.impl == "reference" or not torch.cuda.is_available():
+        print(json.dumps({"impl": args.impl, "unavailable": "the store-only mode times the GPU store"}))
+        return
+    tq.load(build_if_missing=True)
+    dev = torch.device("cuda", 0)
+    preset = args.preset or "turboquant_k3v4_nc"
+    r = time_store_large(dev, presets=(preset,))[preset]
+    if rank == 0:
+        print(json.dumps({"metric": "store Mtok/s", "value": r["mtok_s"], "unit": "Mtok/s",
+                          "preset": preset, "store": r}), flush=True)
+
+
 def main():
     args = _args()
     rank, world, local = _dist()
+    if args.workload == "store_large":
+        run_store_large(args, rank)
+        return
     w = wl.make(args.workload, preset=args.preset, ctx=args.ctx, batch=args.batch)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
