@@ -77,15 +77,20 @@ struct MmaGeom {
     size_t static_smem;   // the kernel's own: the 3-bit keys' pair table
 };
 
-MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G)
+MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len)
 {
     MmaGeom m;
     const SlotGeom g = geom_of(L, soa);
     const int rec = soa ? g.data_bytes : L.slot_size_aligned;   // data bytes per (token, head)
     // FP8-key rows split into CTAs of 4 kv heads (4 records are a whole number
     // of 16-byte copy units): half-size CTAs, four per SM, each waiting on
-    // only 4 warps before a stage is refilled
-    m.hpc = (L.key_fp8 && Hk % 4 == 0 && Hk > 4 && (4 * rec) % 16 == 0 && (!soa || (4 * g.meta_bytes) % 16 == 0))
+    // only 4 warps before a stage is refilled.  With 8 kv heads and long
+    // contexts, CTAs of whole rows copy a page segment at once, which pays
+    // more (32K: 0.334 -> 0.302 ms, 128K: 0.319 -> 0.297 ms; 8K: 0.088 ->
+    // 0.089 ms, A/B on one GB300).
+    const bool full_rows = Hk <= 8 && max_seq_len >= kFullRowsFrom;
+    m.hpc = (L.key_fp8 && Hk % 4 == 0 && Hk > 4 && !full_rows && (4 * rec) % 16 == 0 &&
+             (!soa || (4 * g.meta_bytes) % 16 == 0))
                 ? 4 : Hk;
     m.copy_bytes = m.hpc * rec;
     m.meta_bytes = soa ? m.hpc * g.meta_bytes : 0;
@@ -132,8 +137,10 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
                                          (L.key_bits == 2 && L.value_bits == 2)));
     const bool vals_ok = L.value_bits >= 2 && L.value_bits <= 4;
     if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > kMaxGroup) return false;
-    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
+    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group, 0);
     const int row = m.copy_bytes;
+    // (the whole-row CTAs that FP8 keys with 8 kv heads take at long
+    // contexts copy 1568-byte rows: whole 16-byte units too)
     // Copies are 16-byte units: rows of a multiple of 16 bytes are copied
     // one by one (or per page segment); an AoS CTA that takes whole rows of
     // a multiple of 4 bytes copies whole page segments (16 or 32 rows: a
@@ -144,10 +151,10 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
            2 * kTile * (row + 16 + m.meta_bytes) <= 110 * 1024;
 }
 
-void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int num_sms,
-                      int* ctas_per_split, int* slots)
+void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int max_seq_len,
+                      int num_sms, int* ctas_per_split, int* slots)
 {
-    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
+    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group, max_seq_len);
     *ctas_per_split = num_kv_heads / m.hpc * (group > 4 ? (group + 7) / 8 : 1);
     int n = 0;
     if (num_sms > 0) {
@@ -171,7 +178,8 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
                       long long num_blocks, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
-                      float v_threshold, cudaStream_t st, int stuck_tile, uint32_t wait_polls)
+                      float v_threshold, int max_seq_len, cudaStream_t st, int stuck_tile,
+                      uint32_t wait_polls)
 {
     MmaArgs a;
     a.vthr = v_threshold;
@@ -195,7 +203,7 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
     a.bs = bs;
     a.bs_log2 = bs == 16 ? 4 : bs == 32 ? 5 : bs == 64 ? 6 : 7;
     a.row_bytes = Hk * L.slot_size_aligned;
-    const MmaGeom m = mma_geom(L, soa, Hk, a.G);
+    const MmaGeom m = mma_geom(L, soa, Hk, a.G, max_seq_len);
     a.hpc = m.hpc;
     // groups above 8: CTAs of 8 query heads per kv head, each reading the
     // kv heads' rows (neighbouring CTAs: the second read mostly hits L2)
