@@ -32,164 +32,138 @@ struct DqArgs {
 
 constexpr int kDqWarps = 8;           // warps per CTA, one token at a time each
 
-// Raw packed codes of the lane's 4 dims (every width an LSB-first
-// bitstream): 4-bit: one 16-bit word; 2-bit: one byte; 3-bit: the 16 bits
-// from byte 3*lane/2, whose low 12 (lane even) or high 12 (lane odd) bits
-// are the lane's codes.  Loaded in a first phase so that the loads of
-// several pairs are in flight together.
-template <int BITS>
-struct RawCodes {
-    uint32_t w[1];
-};
-
-template <int BITS>
-__device__ __forceinline__ void load_codes(const uint8_t* p, int lane, RawCodes<BITS>& r)
-{
-    if constexpr (BITS == 2) {
-        r.w[0] = p[lane];
-    } else if constexpr (BITS == 4) {
-        r.w[0] = ld_u16(p + 2 * lane);
-    } else {
-        const uint8_t* q = p + ((3 * lane) >> 1);
-        r.w[0] = uint32_t(q[0]) | (uint32_t(q[1]) << 8);
-    }
-}
-
-// Codes of dims 4 lane .. 4 lane + 3.
-template <int BITS>
-__device__ __forceinline__ void lane_codes(const RawCodes<BITS>& r, int lane, int (&c)[4])
-{
-    if constexpr (BITS == 2) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[i] = (r.w[0] >> (2 * i)) & 3;
-    } else if constexpr (BITS == 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[i] = (r.w[0] >> (4 * i)) & 15;
-    } else {
-        const uint32_t x = r.w[0] >> (4 * (lane & 1));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[i] = (x >> (3 * i)) & 7;
-    }
-}
+// ---------------------------------------------------------------------------
+// Two kv heads per warp at a time: the half-warp hw = lane >> 4 takes heads
+// of its parity and lane l = lane & 15 their dims 8l .. 8l + 7, so the
+// transform takes 4 shuffle stages for two heads at once and every output
+// row is one 16-byte (fp16 / bf16) or two (fp32) stores per lane.
 
 template <typename TO>
-__device__ __forceinline__ void store4(TO* p, const float (&x)[4])
+__device__ __forceinline__ void store8(TO* p, const float (&x)[8])
 {
     if constexpr (sizeof(TO) == 4) {
-        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
     } else {
-        TO t[4];
+        TO t[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) t[i] = from_f32<TO>(x[i]);
-        *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(t);
+        for (int i = 0; i < 8; ++i) t[i] = from_f32<TO>(x[i]);
+        *reinterpret_cast<uint4*>(p) = *reinterpret_cast<const uint4*>(t);
     }
 }
 
-// The slot bytes one lane needs for its 4 dims of one (token, kv head).
-// KBITS: 0 = FP8 keys, 2, 3 or 4 = Lloyd-Max keys.  VBITS: 2, 3 or 4.
+// The slot bytes a lane needs for its 8 dims of one (token, kv head):
+// loaded for two heads per half-warp before either is decoded.
 template <int KBITS, int VBITS>
-struct PairRaw {
-    uint32_t kw;                  // FP8 keys: the lane's 4 key bytes
-    RawCodes<KBITS == 0 ? 4 : KBITS> kc;
-    RawCodes<VBITS> vc;
+struct Raw8 {
+    uint32_t k0, k1;              // key bytes: FP8 8 bytes, else the 16-32 code bits (k0)
+    uint32_t v;                   // value code bits
     uint16_t norm, scale, zero;
 };
 
-// s: the record's data (key data at 0, value data at v_off); m: its metadata
-// (the slot itself for AoS).
-template <int KBITS, int VBITS>
-__device__ __forceinline__ void load_pair(const DqArgs& a, const uint8_t* s, const uint8_t* m, int lane,
-                                          PairRaw<KBITS, VBITS>& r)
+template <int BITS>
+__device__ __forceinline__ uint32_t bits8(const uint8_t* p, int l)
 {
-    if constexpr (KBITS == 0) {
-        r.kw = *reinterpret_cast<const uint32_t*>(s + 4 * lane);   // slot 196 / record 192: 4-byte aligned
+    if constexpr (BITS == 4) {
+        const uint16_t* q = reinterpret_cast<const uint16_t*>(p + 4 * l);
+        return uint32_t(q[0]) | (uint32_t(q[1]) << 16);
+    } else if constexpr (BITS == 2) {
+        return ld_u16(p + 2 * l);
     } else {
-        load_codes<KBITS>(s, lane, r.kc);
-        r.norm = ld_u16(m + a.g.m_norm);
+        static_assert(BITS == 3, "2, 3 or 4 bits");
+        const uint8_t* q = p + 3 * l;
+        return uint32_t(q[0]) | (uint32_t(q[1]) << 8) | (uint32_t(q[2]) << 16);
     }
-    load_codes<VBITS>(s + a.g.v_off, lane, r.vc);
-    r.scale = ld_u16(m + a.g.m_scale);
-    r.zero = ld_u16(m + a.g.m_zero);
 }
 
-// Lane l of the warp writes dims 4l .. 4l+3 of one kv head's K and V rows.
-template <typename TO, int KBITS, int VBITS>
-__device__ __forceinline__ void finish_pair(const DqArgs& a, TO* ko, TO* vo, int lane, float cl,
-                                            const float (&sg4)[4], const PairRaw<KBITS, VBITS>& r)
+template <int KBITS, int VBITS>
+__device__ __forceinline__ void load8(const DqArgs& a, const uint8_t* dp, const uint8_t* mp, int l,
+                                      Raw8<KBITS, VBITS>& r)
 {
-    float k[4], v[4];
+    if constexpr (KBITS == 0) {
+        const uint16_t* q = reinterpret_cast<const uint16_t*>(dp + 8 * l);
+        r.k0 = uint32_t(q[0]) | (uint32_t(q[1]) << 16);
+        r.k1 = uint32_t(q[2]) | (uint32_t(q[3]) << 16);
+    } else {
+        r.k0 = bits8<KBITS>(dp, l);
+        r.norm = ld_u16(mp + a.g.m_norm);
+    }
+    r.v = bits8<VBITS>(dp + a.g.v_off, l);
+    r.scale = ld_u16(mp + a.g.m_scale);
+    r.zero = ld_u16(mp + a.g.m_zero);
+}
+
+template <typename TO, int KBITS, int VBITS>
+__device__ __forceinline__ void decode8(const Raw8<KBITS, VBITS>& r, int l, float cl, const float (&sg)[8],
+                                        TO* kr, TO* vr, bool live)
+{
+    float k[8], v[8];
     if constexpr (KBITS == 0) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = i < 4 ? r.k0 : r.k1;
             const __half_raw hr = __nv_cvt_fp8_to_halfraw(
-                static_cast<__nv_fp8_storage_t>((r.kw >> (8 * i)) & 0xFF), __NV_E4M3);
+                static_cast<__nv_fp8_storage_t>((w >> (8 * (i & 3))) & 0xFF), __NV_E4M3);
             k[i] = __half2float(__half(hr));
         }
     } else {
-        int c[4];
-        lane_codes<KBITS>(r.kc, lane, c);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) k[i] = __shfl_sync(0xffffffffu, cl, c[i]);
-        fwht128_warp(k, lane);                   // H c up to the 1/sqrt(D) factor
+        for (int i = 0; i < 8; ++i)
+            k[i] = __shfl_sync(0xffffffffu, cl, (r.k0 >> (KBITS * i)) & ((1u << KBITS) - 1));
+        fwht128_half(k, l);                      // H c up to the 1/sqrt(D) factor
         const float f = __half2float(__ushort_as_half(r.norm)) * 0.08838834764831845f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) k[i] = k[i] * f * sg4[i];
+        for (int i = 0; i < 8; ++i) k[i] = k[i] * f * sg[i];
     }
-    {
-        const float sc = __half2float(__ushort_as_half(r.scale));
-        const float z = __half2float(__ushort_as_half(r.zero));
-        int c[4];
-        lane_codes<VBITS>(r.vc, lane, c);
+    const float sc = __half2float(__ushort_as_half(r.scale));
+    const float z = __half2float(__ushort_as_half(r.zero));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = fmaf(float(c[i]), sc, z);   // code * scale is exact in fp32
+    for (int i = 0; i < 8; ++i)
+        v[i] = fmaf(float((r.v >> (VBITS * i)) & ((1u << VBITS) - 1)), sc, z);   // code * scale is exact in fp32
+    if (live) {
+        store8(kr, k);
+        store8(vr, v);
     }
-    store4(ko + 4 * lane, k);
-    store4(vo + 4 * lane, v);
 }
 
-// Warps stride over tokens; a warp does every kv head of its token, two
-// heads per step with the slot loads of both issued before either is decoded.
+// A warp per token (grid-stride over tokens), two head pairs per step with
+// the slot loads of both issued before either is decoded.
 template <typename TO, int KBITS, int VBITS>
-__global__ void __launch_bounds__(32 * kDqWarps) dequant_kernel(DqArgs a)
+__global__ void __launch_bounds__(32 * kDqWarps) dequant2_kernel(DqArgs a)
 {
-    const int lane = threadIdx.x & 31;
-    const long long nw = (long long)gridDim.x * kDqWarps;
-    // centroid table in registers: lane j < 2^KBITS holds c[j]; the lane's signs
-    const float cl = (KBITS > 0 && lane < (1 << KBITS)) ? a.centroids[lane] : 0.f;
-    float sg4[4] = {1.f, 1.f, 1.f, 1.f};
-    if constexpr (KBITS > 0) {
+    const int lane = threadIdx.x & 31, hw = lane >> 4, l = lane & 15;
+    // centroid table in registers: lane j of each half holds c[j]; the lane's signs
+    const float cl = (KBITS > 0 && l < (1 << KBITS)) ? a.centroids[l] : 0.f;
+    float sg[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sg4[i] = float(a.signs[4 * lane + i]);
-    }
-    const int Hk = a.Hk, S = a.g.slot;
+    for (int i = 0; i < 8; ++i) sg[i] = KBITS > 0 ? float(a.signs[8 * l + i]) : 1.f;
+    const int Hk = a.Hk;
+    const long long nw = (long long)gridDim.x * kDqWarps;
     for (long long n = (long long)blockIdx.x * kDqWarps + (threadIdx.x >> 5); n < a.num_tokens; n += nw) {
         const long long slot = a.slot_mapping[n];
-        TO* kr = static_cast<TO*>(a.kout) + n * a.k_stride;
-        TO* vr = static_cast<TO*>(a.vout) + n * a.v_stride;
-        if (slot < 0 || slot >= a.nslots) {     // padding: zero rows, nothing read
-            const float z[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int h = 0; h < Hk; ++h) {
-                store4(kr + h * kHeadDim + 4 * lane, z);
-                store4(vr + h * kHeadDim + 4 * lane, z);
+        TO* kbase = static_cast<TO*>(a.kout) + n * a.k_stride + 8 * l;
+        TO* vbase = static_cast<TO*>(a.vout) + n * a.v_stride + 8 * l;
+        if (slot < 0 || slot >= a.nslots) {       // padding: zero rows, nothing read
+            const float zr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int h = hw; h < Hk; h += 2) {
+                store8(kbase + h * kHeadDim, zr);
+                store8(vbase + h * kHeadDim, zr);
             }
             continue;
         }
-        // the token's records: data at dbase + h * ds, metadata at mbase + h * ms
-        const uint8_t *dbase, *mbase;
-        slot_ptrs(a.g, a.cache, slot / a.bs, int(slot % a.bs), 0, a.bs, Hk, dbase, mbase);
-        const int ds = a.g.soa ? a.g.data_bytes : S, ms = a.g.soa ? a.g.meta_bytes : S;
-        int h = 0;
-        for (; h + 1 < Hk; h += 2) {
-            PairRaw<KBITS, VBITS> r0, r1;
-            load_pair(a, dbase + h * ds, mbase + h * ms, lane, r0);
-            load_pair(a, dbase + (h + 1) * ds, mbase + (h + 1) * ms, lane, r1);
-            finish_pair<TO>(a, kr + h * kHeadDim, vr + h * kHeadDim, lane, cl, sg4, r0);
-            finish_pair<TO>(a, kr + (h + 1) * kHeadDim, vr + (h + 1) * kHeadDim, lane, cl, sg4, r1);
-        }
-        if (h < Hk) {
-            PairRaw<KBITS, VBITS> r0;
-            load_pair(a, dbase + h * ds, mbase + h * ms, lane, r0);
-            finish_pair<TO>(a, kr + h * kHeadDim, vr + h * kHeadDim, lane, cl, sg4, r0);
+        const long long page = slot / a.bs;
+        const int off = int(slot - page * a.bs);
+        for (int h0 = 0; h0 < Hk; h0 += 4) {
+            const int ha = h0 + hw, hb = h0 + 2 + hw;      // this half-warp's two heads
+            const bool la = ha < Hk, lb = hb < Hk;        // an odd count leaves halves idle
+            const uint8_t *dpa, *mpa, *dpb, *mpb;
+            slot_ptrs(a.g, a.cache, page, off, la ? ha : 0, a.bs, Hk, dpa, mpa);
+            slot_ptrs(a.g, a.cache, page, off, lb ? hb : 0, a.bs, Hk, dpb, mpb);
+            Raw8<KBITS, VBITS> ra, rb;
+            load8(a, dpa, mpa, l, ra);
+            load8(a, dpb, mpb, l, rb);
+            decode8<TO>(ra, l, cl, sg, kbase + ha * kHeadDim, vbase + ha * kHeadDim, la);
+            decode8<TO>(rb, l, cl, sg, kbase + hb * kHeadDim, vbase + hb * kHeadDim, lb);
         }
     }
 }
@@ -209,7 +183,7 @@ cudaError_t launch_one(const DqArgs& a, long long tokens, cudaStream_t st)
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dequant_kernel<TO, KBITS, VBITS>,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dequant2_kernel<TO, KBITS, VBITS>,
                                                               32 * kDqWarps, 0);
         if (e != cudaSuccess) return e;
         n = per_sm > 0 && sms > 0 ? per_sm * sms : 1;
@@ -217,7 +191,7 @@ cudaError_t launch_one(const DqArgs& a, long long tokens, cudaStream_t st)
     }
     long long grid = (tokens + kDqWarps - 1) / kDqWarps;
     if (grid > n) grid = n;
-    dequant_kernel<TO, KBITS, VBITS><<<unsigned(grid), 32 * kDqWarps, 0, st>>>(a);
+    dequant2_kernel<TO, KBITS, VBITS><<<unsigned(grid), 32 * kDqWarps, 0, st>>>(a);
     return cudaGetLastError();
 }
 

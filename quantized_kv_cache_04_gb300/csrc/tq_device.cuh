@@ -58,6 +58,33 @@ __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane)
     }
 }
 
+// Unnormalised Sylvester Walsh-Hadamard transform of a 128-vector held 8
+// consecutive elements per lane of a half-warp (element 8l + i is v[i]):
+// index bits 0-2 inside the lane, bits 3-6 across lanes.  Each butterfly
+// maps (x_lo, x_hi) -> (x_lo + x_hi, x_lo - x_hi); across lanes the upper
+// partner computes fma(x, -1, p) = p - x and the lower fma(x, 1, p) = x + p.
+__device__ __forceinline__ void fwht128_half(float (&v)[8], int l)
+{
+#pragma unroll
+    for (int b = 1; b < 8; b <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (!(i & b)) {
+                const float x = v[i], y = v[i + b];
+                v[i] = x + y;
+                v[i + b] = x - y;
+            }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+        const float sg = (l & m) ? -1.f : 1.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float p = __shfl_xor_sync(0xffffffffu, v[i], m);
+            v[i] = __fmaf_rn(v[i], sg, p);
+        }
+    }
+}
+
 __device__ __forceinline__ uint16_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
 }  // namespace tq
