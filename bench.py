@@ -215,7 +215,7 @@ def kernel_source_hash() -> str:
     """Hash of the decode kernels' sources (both stages, both stage-1 paths)."""
     h = hashlib.sha256()
     for f in ("tq_decode.cu", "tq_decode_mma.cu", "tq_decode_mma.cuh", "tq_decode_mma_sparse.cu",
-              "tq_internal.h"):
+              "tq_internal.h", "tq_device.cuh"):
         h.update(open(os.path.join(ROOT, "quantized_kv_cache_04_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

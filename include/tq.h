@@ -15,11 +15,11 @@
  * Slot interior (byte offsets in tq_layout):
  *   [key data][k_norm fp16, MSE presets only][value data][v_scale fp16][v_zero fp16][pad to even]
  * key data is either D bytes of FP8 E4M3 (k8v4) or a b_k-bit packed code
- * stream; value data is a b_v-bit packed code stream.  4-bit codes: two per
- * byte, low nibble first.  3-bit codes (8 per 3 bytes): groups of 32 codes
- * in 12 bytes read as little-endian 32-bit words W0, W1, W2; code 8w+i
- * (i < 8, w < 3) sits in bits [4i, 4i+3) of Ww and bit w of code 24+i in bit
- * 4i+3 of Ww, so every code starts on a nibble boundary.  Sizes per
+ * stream; value data is a b_v-bit packed code stream.  Every code stream is
+ * LSB-first little-endian: code i occupies bits [b*i, b*i + b).  4-bit
+ * codes: two per byte, low nibble first; 2-bit: four per byte; 3-bit: 8
+ * codes per 3 bytes ("turboquant-plus.md", Background), e.g. codes 0..7 ->
+ * bytes 0x88 0xC6 0xFA.  Sizes per
  * "vllm.v1.attention.backends.turboquant_attn" API page,
  * section "__init__" (mse bytes, value data bytes) and section
  * "_continuation_prefill" (field order k_norm, v_scale, v_zero).

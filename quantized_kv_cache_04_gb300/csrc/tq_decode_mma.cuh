@@ -773,7 +773,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // maps to dims
     //   FP8 keys:   16 kk + 4 tig + j   one key word per k-step, bank-conflict
     //               free across the warp
-    //   3-bit keys: 32 tig + 4 kk + j   one 32-code group (three words) per thread
+    //   3-bit keys: 32 tig + 4 kk + j   12 bytes (32 codes) per thread and row
     //   4-bit keys: the same, 16 bytes per thread
     //   2-bit keys: 32 tig + 16 (kk >> 2) + 8 (kk & 1) + ((kk >> 1) & 1) + 2 j
     //               (8 bytes per thread; see qk_tile)
