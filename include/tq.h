@@ -215,7 +215,7 @@ size_t tq_decode_workspace_bytes(int batch, int num_q_heads, int num_splits, int
  *     k_norm * <q_rot, c[idx]> (MSE) or softmax_scale * <q, k_fp8> (k8v4);
  *     online softmax; v_hat = code * v_scale + v_zero accumulated.
  *     Splits are consecutive token ranges (the tensor-core kernel rounds
- *     their length up to whole 16-token tiles); the result does not depend
+ *     their length up to whole 32-token tiles); the result does not depend
  *     on the split count beyond rounding.
  *   stage 2: o = sum_s w_s o_s / sum_s w_s, w_s = exp(lse_s - max lse),
  *     lse = max + ln sum w_s (natural log, scale included).
