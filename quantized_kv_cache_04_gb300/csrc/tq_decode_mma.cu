@@ -74,7 +74,7 @@ float two_bit_alpha()
 struct MmaGeom {
     int hpc, copy_bytes, smem_row, meta_bytes, nstages;
     size_t smem;          // dynamic shared memory
-    size_t static_smem;   // the kernel's own: the 3-bit keys' pair table
+    size_t static_smem;   // the kernel's own: the 3- or 4-bit keys' pair table
 };
 
 MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len)
@@ -101,10 +101,11 @@ MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len)
     // ring budget: two CTAs of 8 kv-head warps, or four CTAs of 4 warps, per
     // SM (about 16 warps); fewer kv heads take a proportional share (at
     // least 28 KB), so that CTAs of 2 or 4 warps still fill an SM.  MSE keys
-    // with G = 8 also keep 4 KB of q fragments per warp, and 3-bit keys hold
-    // their 8 KB pair table in static shared memory
+    // with G = 8 also keep 4 KB of q fragments per warp, and 3- and 4-bit
+    // keys hold their pair table (8 / 32 KB) in static shared memory
     const int qsm = (!L.key_fp8 && G > 4) ? m.hpc * 4096 : 0;
-    m.static_smem = (!L.key_fp8 && L.key_bits == 3) ? size_t(kLut3Entries) * 8 : 0;
+    m.static_smem = L.key_fp8 ? 0 : L.key_bits == 3 ? size_t(kLut3Entries) * 8
+                                   : L.key_bits == 4 ? size_t(kLut4Entries) * 8 : 0;
     const int budget = m.hpc < Hk ? 56 * 1024 : (Hk >= 8 ? 100 * 1024 : std::max(28 * 1024, 100 * 1024 * Hk / 8));
     int nst = (budget + (qsm ? 12 * 1024 : 0) - qsm - int(m.static_smem)) / stage;
     nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);

@@ -213,9 +213,27 @@ __device__ __forceinline__ uint32_t pair_off(const uint32_t (&w)[3], int bit)
     return x & 0x1F80u;
 }
 
-__device__ __forceinline__ uint2 lut_pair(const uint2* lut, const uint32_t (&w)[3], int p, uint32_t l8)
+// 4-bit keys: the code pair of byte p of the group's 16 bytes (codes 2p in
+// the low nibble, 2p + 1 in the high one) indexes a 256-entry table laid out
+// like the 3-bit one (entries 128 bytes apart, a copy per half-warp lane):
+// the byte is shifted to bits [7, 15).
+constexpr int kLut4Entries = 256 * 16;
+
+__device__ __forceinline__ uint32_t pair_off(const uint32_t (&w)[4], int p)
 {
-    return *reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(lut) + (pair_off(w, 6 * p) | l8));
+    const uint32_t x = w[p >> 2];
+    const int b = 8 * (p & 3);
+    return (b >= 7 ? x >> (b - 7) : x << (7 - b)) & 0x7F80u;
+}
+
+// the (hi, lo) entry of code pair p of a 3-bit (N = 3) or 4-bit (N = 4) group
+template <int N>
+__device__ __forceinline__ uint2 lut_pair(const uint2* lut, const uint32_t (&w)[N], int p, uint32_t l8)
+{
+    uint32_t off;
+    if constexpr (N == 3) off = pair_off(w, 6 * p);
+    else                  off = pair_off(w, p);
+    return *reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(lut) + (off | l8));
 }
 
 // Longest-first dispatch: CTA row y (blockIdx.y) takes the sequence of rank y
@@ -265,55 +283,11 @@ __device__ __forceinline__ void cvt_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& h
         : "r"(w));
 }
 
-// 16-entry centroid lookup (4-bit keys) of the four codes in the low 16 bits
-// of s (code j in nibble j).  PRMT indexes 8 bytes, so each byte plane has a
-// table for codes 0-7 (T[2p]) and one for codes 8-15 (T[2p + 1]); both are
-// read with the low 3 bits of every code and a third PRMT keeps, per byte,
-// the one that bit 3 names.  Planes: 0/1 = low/high byte of fp16(c), 2/3 =
-// low/high byte of the fp16 residual.  h0/h1 (l0/l1): the hi (lo) halves of
-// codes 0,1 and 2,3 as half2.
-__device__ __forceinline__ void lut16(const uint32_t (&T)[8][2], uint32_t s, uint32_t& h0, uint32_t& h1,
-                                      uint32_t& l0, uint32_t& l1)
-{
-    const uint32_t s7 = s & 0x7777u;
-    const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;   // byte j from the second word if bit 3 set
-    uint32_t x[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-        x[p] = prmt(prmt(T[2 * p][0], T[2 * p][1], s7), prmt(T[2 * p + 1][0], T[2 * p + 1][1], s7), pick);
-    h0 = prmt(x[0], x[1], 0x5140u);
-    h1 = prmt(x[0], x[1], 0x7362u);
-    l0 = prmt(x[2], x[3], 0x5140u);
-    l1 = prmt(x[2], x[3], 0x7362u);
-}
-
-// The same lookup for a symmetric codebook (c_k = -c_(15-k), the Lloyd-Max
-// case): an 8-entry magnitude table per byte plane (T[0] / T[1]: low / high
-// byte of fp16(M_j), T[2] / T[3]: of the fp16 residual, M_j = c_(8+j)) read
-// with j = (code & 7) ^ (bit 3 ? 0 : 7), and the sign of the codes below 8
-// put into the high bytes: PRMT's sign-replicate mode turns each code's bit
-// 3 into a 0x00 / 0xFF byte (bit 3 of codes 0 / 2 is the top bit of bytes
-// 0 / 1 of s << 4, of codes 1 / 3 the top bit of bytes 0 / 1 of s).
-// 15 instructions for four codes against 19.
-__device__ __forceinline__ void lut16_sym(const uint32_t (&T)[8][2], uint32_t s, uint32_t& h0, uint32_t& h1,
-                                          uint32_t& l0, uint32_t& l1)
-{
-    const uint32_t t = (~s >> 3) & 0x1111u;               // 1 where bit 3 is clear
-    const uint32_t j = (s & 0x7777u) ^ (t * 7u);          // magnitude index
-    const uint32_t pos = prmt(s << 4, s, 0xD9C8u);        // 0xFF where bit 3 is set
-    const uint32_t neg = ~pos & 0x80808080u;              // fp16 sign bits of the high bytes
-    const uint32_t p0 = prmt(T[0][0], T[0][1], j), p1 = prmt(T[1][0], T[1][1], j) ^ neg;
-    const uint32_t u0 = prmt(T[2][0], T[2][1], j), u1 = prmt(T[3][0], T[3][1], j) ^ neg;
-    h0 = prmt(p0, p1, 0x5140u);
-    h1 = prmt(p0, p1, 0x7362u);
-    l0 = prmt(u0, u1, 0x5140u);
-    l1 = prmt(u0, u1, 0x7362u);
-}
-
-// Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1: row gid+8).
-// Returns the raw accumulators: G = 4 -> sc (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).
-// MSE keys with G = 8 read their q fragments from shared memory (qsm: this
-// lane's uint4 of k-step 0, stride 32).
+// Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1:
+// row gid+8), FP8 or 2-bit keys.  Returns the raw accumulators: G = 4 -> sc
+// (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).  2-bit keys with
+// G = 8 read their q fragments from shared memory (qsm: this lane's uint4 of
+// k-step 0, stride 32).
 template <int KMODE, int G, bool KGEN, int KM, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
@@ -333,60 +307,13 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
             mma16816(sc[kk & 1], A, bq[kk][0], bq[kk][1]);
             if constexpr (G == 8) mma16816(scl[kk & 1], A, bql[kk][0], bql[kk][1]);
         }
-    } else if constexpr (KMODE == 3) {
-        // 3-bit keys: the MMA's 16 rows are 8 tokens x {hi, lo}: row gid
-        // holds token gid's fp16 centroids, row gid + 8 their fp16
-        // residuals, so one table load (a code pair's hi and lo words) is
-        // A registers a0 / a1 (pair 2 kk, columns 2 tig, 2 tig + 1) or a2 / a3
-        // (pair 2 kk + 1, columns 2 tig + 8, 2 tig + 9) as loaded.  The
-        // thread's two tokens (rows r0, r1; the thread's 32 codes of each,
-        // dims 32 tig .. 32 tig + 31, are 12 bytes) run as two such MMAs per
-        // k-step, and a token's score is the sum of its hi and lo rows.
-        uint32_t w0[3], w1[3];
-        lds_words<3, KM>(r0 + 12 * tig, kmis, w0);
-        lds_words<3, KM>(r1 + 12 * tig, kmis, w1);
-        constexpr int NC = G == 4 ? 2 : 1;    // accumulator chains per token and q part
-        float c0[NC][4] = {}, c1[NC][4] = {}, d0[4] = {}, d1[4] = {};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint2 e0 = lut_pair(lut, w0, 2 * kk, l8), e1 = lut_pair(lut, w0, 2 * kk + 1, l8);
-            const uint2 f0 = lut_pair(lut, w1, 2 * kk, l8), f1 = lut_pair(lut, w1, 2 * kk + 1, l8);
-            const uint32_t A0[4] = {e0.x, e0.y, e1.x, e1.y};
-            const uint32_t A1[4] = {f0.x, f0.y, f1.x, f1.y};
-            if constexpr (G == 4) {            // columns: head x {q hi, q lo}
-                mma16816(c0[kk & 1], A0, bq[kk][0], bq[kk][1]);
-                mma16816(c1[kk & 1], A1, bq[kk][0], bq[kk][1]);
-            } else {                           // columns: 8 heads; q hi and q lo in two MMAs
-                const uint4 qf = qsm[32 * kk];
-                mma16816(c0[0], A0, qf.x, qf.y);
-                mma16816(c1[0], A1, qf.x, qf.y);
-                mma16816(d0, A0, qf.z, qf.w);
-                mma16816(d1, A1, qf.z, qf.w);
-            }
-        }
-        // out / outl in the layout of the 16-token form: [0] / [1] = token r0,
-        // columns 2 tig / 2 tig + 1; [2] / [3] = token r1
-#pragma unroll
-        for (int j = 1; j < NC; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { c0[0][i] += c0[j][i]; c1[0][i] += c1[j][i]; }
-        out[0] = c0[0][0] + c0[0][2];
-        out[1] = c0[0][1] + c0[0][3];
-        out[2] = c1[0][0] + c1[0][2];
-        out[3] = c1[0][1] + c1[0][3];
-        outl[0] = d0[0] + d0[2];
-        outl[1] = d0[1] + d0[3];
-        outl[2] = d1[0] + d1[2];
-        outl[3] = d1[1] + d1[3];
-        return;
     } else {
-        // one 32-code group (4-bit: 16 bytes, 2-bit: 8 bytes) of each row per
-        // thread, as four nibble words of 8 codes (k-step kk uses 4 of them)
+        // 2-bit keys: one 32-code group (8 bytes) of each row per thread.
+        // The 32 codes = two words; the even codes of a word go to one
+        // nibble word and the odd codes to another (code 2i / 2i + 1 of the
+        // word in nibble i), so k-step kk covers dims with stride 2
         uint32_t c0[4], c1[4];
-        if constexpr (KMODE == 2) {
-            // 32 two-bit codes = two words; the even codes of a word go to one
-            // nibble word and the odd codes to another (code 2i / 2i + 1 of
-            // the word in nibble i), so k-step kk covers dims with stride 2
+        {
             uint32_t w0[2], w1[2];
             lds_words<2, KM>(r0 + 8 * tig, kmis, w0);
             lds_words<2, KM>(r1 + 8 * tig, kmis, w1);
@@ -397,25 +324,16 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
                 c1[2 * i] = w1[i] & 0x33333333u;
                 c1[2 * i + 1] = (w1[i] >> 2) & 0x33333333u;
             }
-        } else {
-            lds_words<4, KM>(r0 + 16 * tig, kmis, c0);
-            lds_words<4, KM>(r1 + 16 * tig, kmis, c1);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t s0 = c0[kk >> 1] >> (16 * (kk & 1));
             const uint32_t s1 = c1[kk >> 1] >> (16 * (kk & 1));
             uint32_t Ahi[4], Alo[4] = {0u, 0u, 0u, 0u};
-            constexpr bool use_lo = KMODE != 2 || KGEN;   // 2-bit keys may need no lo part
-            if constexpr (KMODE == 4 && KGEN) {
-                lut16(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
-                lut16(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
-            } else if constexpr (KMODE == 4) {
-                lut16_sym(T, s0, Ahi[0], Ahi[2], Alo[0], Alo[2]);
-                lut16_sym(T, s1, Ahi[1], Ahi[3], Alo[1], Alo[3]);
-            } else {
-                // 2-bit keys: one lookup per byte plane, then interleave
-                // the low and high bytes into half2 registers
+            constexpr bool use_lo = KGEN;     // fp16-exact alpha * c_k: no lo part
+            {
+                // one lookup per byte plane, then interleave the low and
+                // high bytes into half2 registers
                 const uint32_t p0 = prmt(T[0][0], T[0][1], s0), p1 = prmt(T[1][0], T[1][1], s0);
                 const uint32_t q0 = prmt(T[0][0], T[0][1], s1), q1 = prmt(T[1][0], T[1][1], s1);
                 Ahi[0] = prmt(p0, p1, 0x5140u);
@@ -453,18 +371,26 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
     }
 }
 
-// 3-bit keys, both 16-row tiles at once: the four tokens of the thread
-// (rows r[0..3] = tokens gid, gid + 8 of tile 0, then of tile 1) in one
-// k-step loop, so the lookups and MMAs of the two tiles interleave.
-// out[rt] / outl[rt] as qk_tile's.
-template <int G, int KM>
-__device__ __forceinline__ void qk_tile3x2(const uint8_t* const (&r)[4], int tig, int kmis,
-                                           const uint32_t (&bq)[8][2], const uint4* qsm, const uint2* lut,
-                                           uint32_t l8, float (&out)[2][4], float (&outl)[2][4])
+// 3- and 4-bit keys (KB bits per code) through the pair table: the MMA's
+// 16 rows are 8 tokens x {hi, lo}: row gid holds token gid's fp16 centroids
+// and row gid + 8 their fp16 residuals, so one table load (a code pair's hi
+// and lo words) is A registers a0 / a1 (pair 2 kk, columns 2 tig, 2 tig + 1)
+// or a2 / a3 (pair 2 kk + 1, columns 2 tig + 8, 2 tig + 9) as loaded, and a
+// token's score is the sum of its hi and lo rows.  The thread's 32 codes of
+// a token (dims 32 tig .. 32 tig + 31) are 4 KB bytes (12 or 16).  Both 16-row tiles
+// at once: the thread's four tokens (rows r[0..3] = tokens gid, gid + 8 of
+// tile 0, then of tile 1) share one k-step loop, so the lookups and MMAs of
+// the two tiles interleave.  out[rt]: G = 4 -> columns head x {q hi, q lo};
+// G = 8 -> q hi (out) and q lo (outl) of 8 heads; [0] / [1] = token gid,
+// columns 2 tig / 2 tig + 1; [2] / [3] = token gid + 8.
+template <int KB, int G, int KM>
+__device__ __forceinline__ void qk_pairs(const uint8_t* const (&r)[4], int tig, int kmis,
+                                         const uint32_t (&bq)[8][2], const uint4* qsm, const uint2* lut,
+                                         uint32_t l8, float (&out)[2][4], float (&outl)[2][4])
 {
-    uint32_t w[4][3];
+    uint32_t w[4][KB];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) lds_words<3, KM>(r[i] + 12 * tig, kmis, w[i]);
+    for (int i = 0; i < 4; ++i) lds_words<KB, KM>(r[i] + 4 * KB * tig, kmis, w[i]);
     float c[4][4] = {}, d[4][4] = {};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -629,7 +555,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     // 3-bit keys: the code-pair centroid table (8 KB; one element elsewhere)
-    __shared__ __align__(16) uint2 key_lut[KMODE == 3 ? kLut3Entries : 1];
+    __shared__ __align__(16) uint2 key_lut[KMODE == 3 ? kLut3Entries : KMODE == 4 ? kLut4Entries : 1];
     // launched as a programmatic dependent of the previous kernel in the
     // stream (typically the store of the step's new tokens): wait for it to
     // complete before the first read of global memory
@@ -795,15 +721,17 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         if (err <= 5e-7f) { key_alpha = al; key_lo = false; }
     }
 
-    // 3-bit keys: entry e (codes e & 7 and e >> 3) of the pair table holds
-    // fp16x2 (hi) and fp16x2 (lo) of the two centroids, once per half-warp
-    // lane; the barrier after the q staging below orders it before any use
-    if constexpr (KMODE == 3) {
-        for (int i = threadIdx.x; i < kLut3Entries; i += blockDim.x) {
+    // 3- and 4-bit keys: entry e (codes e mod 2^bits and e >> bits) of the
+    // pair table holds fp16x2 (hi) and fp16x2 (lo) of the two centroids, once
+    // per half-warp lane; the barrier after the q staging below orders it
+    // before any use
+    if constexpr (KMODE == 3 || KMODE == 4) {
+        constexpr int NE = KMODE == 3 ? kLut3Entries : kLut4Entries;
+        for (int i = threadIdx.x; i < NE; i += blockDim.x) {
             const int e = i >> 4;
             float h0, l0, h1, l1;
-            split_f16(a.centroids[e & 7], h0, l0);
-            split_f16(a.centroids[e >> 3], h1, l1);
+            split_f16(a.centroids[e & ((1 << KMODE) - 1)], h0, l0);
+            split_f16(a.centroids[e >> KMODE], h1, l1);
             key_lut[i] = make_uint2(pack_half2(h0, h1), pack_half2(l0, l1));
         }
     }
@@ -875,48 +803,23 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     if (warp == 0)
         for (int i = s_q; i < NST; ++i) issue(i, i);
 
-    // ---------------- centroid byte planes for the PRMT lookup (2- and 4-bit
-    // keys): plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte
-    // of the fp16 residual c - fp16(c), with c = key_alpha * c_k.  2-bit keys:
-    // T[p][k >> 2] holds entries 4(k>>2) .. 4(k>>2)+3 of plane p.  4-bit keys: T[2p + (k >> 3)] holds
-    // plane p of codes 8(k>>3) .. 8(k>>3)+7 in the same way.
-    // 4-bit keys with a symmetric codebook (c_k = -c_(15-k) bit for bit; the
-    // same test in every thread) use the 8-entry magnitude planes instead.
-    bool key_sym = false;
-    if constexpr (KMODE == 4) {
-        key_sym = true;
+    // ---------------- centroid byte planes for the PRMT lookup (2-bit keys):
+    // plane 0/1 = low/high byte of fp16(c), plane 2/3 = low/high byte of the
+    // fp16 residual c - fp16(c), with c = key_alpha * c_k; T[p][0] holds the
+    // four codes' bytes of plane p
+    uint32_t T[4][2] = {};
+    if constexpr (KMODE == 2) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) key_sym &= a.centroids[k] == -a.centroids[15 - k];
-    }
-    uint32_t T[KMODE == 4 ? 8 : 4][2] = {};
-    if (KMODE == 4 && key_sym) {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const float c = a.centroids[8 + m];
-            const __half chi = __float2half_rn(c);
-            const __half clo = __float2half_rn(c - __half2float(chi));
-            const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
-            const int sh = 8 * (m & 3), w = m >> 2;
-            T[0][w] |= (hb & 0xFFu) << sh;
-            T[1][w] |= (hb >> 8) << sh;
-            T[2][w] |= (lb & 0xFFu) << sh;
-            T[3][w] |= (lb >> 8) << sh;
-        }
-    } else if constexpr (KMODE == 2 || KMODE == 4) {
-        constexpr int NC = 1 << KMODE;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
+        for (int k = 0; k < 4; ++k) {
             const float c = key_alpha * a.centroids[k];
             const __half chi = __float2half_rn(c);
             const __half clo = __float2half_rn(c - __half2float(chi));
             const uint32_t hb = __half_as_ushort(chi), lb = __half_as_ushort(clo);
-            const int sh = 8 * (k & 3), w = (k >> 2) & 1;
-            const int t = KMODE == 4 ? (k >> 3) : 0;     // table of the plane
-            const int st = KMODE == 4 ? 2 : 1;           // tables per plane
-            T[0 * st + t][w] |= (hb & 0xFFu) << sh;
-            T[1 * st + t][w] |= (hb >> 8) << sh;
-            T[2 * st + t][w] |= (lb & 0xFFu) << sh;
-            T[3 * st + t][w] |= (lb >> 8) << sh;
+            const int sh = 8 * k;
+            T[0][0] |= (hb & 0xFFu) << sh;
+            T[1][0] |= (hb >> 8) << sh;
+            T[2][0] |= (lb & 0xFFu) << sh;
+            T[3][0] |= (lb >> 8) << sh;
         }
     }
 
@@ -941,7 +844,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // One 32-token tile in stage memory st (this warp's slot at offset 0).
     // PARTIAL: some of its tokens lie at or past t_end and are masked.
     // KGEN: the general key path; false: 2-bit keys without the lo part
-    // (key_alpha), 4-bit keys read through the symmetric lookup (key_sym)
+    // (key_alpha)
     // KM / VM: the key / value misalignment of this warp's slot (0 or 2)
     auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag, auto lo_tag,
                     auto km_tag, auto vm_tag) {
@@ -952,10 +855,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         float s[NH][2][2], vs[2][2], vz[2][2];
         bool ok[2][2];
         [[maybe_unused]] float sc2[2][4], scl2[2][4];
-        if constexpr (KMODE == 3) {
+        if constexpr (KMODE == 3 || KMODE == 4) {
             const uint8_t* const rr[4] = {st + tau0 * rs, st + tau1 * rs, st + (16 + tau0) * rs,
                                           st + (16 + tau1) * rs};
-            qk_tile3x2<G, KM>(rr, tig, kmis, bq, qsm, key_lut, l8, sc2, scl2);
+            qk_pairs<KMODE, G, KM>(rr, tig, kmis, bq, qsm, key_lut, l8, sc2, scl2);
         }
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt) {
@@ -964,7 +867,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
-            if constexpr (KMODE == 3) {
+            if constexpr (KMODE == 3 || KMODE == 4) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) { sc[i] = sc2[rt][i]; scl[i] = scl2[rt][i]; }
             } else {
@@ -1122,7 +1025,6 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     };
     int failed_at;
     if constexpr (KMODE == 2) failed_at = key_lo ? run_mis(std::true_type{}) : run_mis(std::false_type{});
-    else if constexpr (KMODE == 4) failed_at = key_sym ? run_mis(std::false_type{}) : run_mis(std::true_type{});
     else                      failed_at = run_mis(std::true_type{});
     // stage 2 (a programmatic dependent launch) may start its launch now; it
     // waits for this grid's completion before it reads the partials
