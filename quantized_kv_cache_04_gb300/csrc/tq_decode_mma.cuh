@@ -391,35 +391,40 @@ __device__ __forceinline__ void qk_pairs(const uint8_t* const (&r)[4], int tig, 
     uint32_t w[4][KB];
 #pragma unroll
     for (int i = 0; i < 4; ++i) lds_words<KB, KM>(r[i] + 4 * KB * tig, kmis, w[i]);
-    float c[4][4] = {}, d[4][4] = {};
+    // G = 8: the q lo part meets only the keys' hi words, as one MMA over
+    // the 16 tokens of a row tile (rows = tokens gid, gid + 8); the term it
+    // leaves out, k lo . q lo, is below 2^-22 of |k| |q|
+    float c[4][4] = {}, d[2][4] = {};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         uint4 qf;
         if constexpr (G == 8) qf = qsm[32 * kk];
+        uint2 e0[4], e1[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint2 e0 = lut_pair(lut, w[i], 2 * kk, l8), e1 = lut_pair(lut, w[i], 2 * kk + 1, l8);
-            const uint32_t A[4] = {e0.x, e0.y, e1.x, e1.y};
-            if constexpr (G == 4) {
-                mma16816(c[i], A, bq[kk][0], bq[kk][1]);
-            } else {
-                mma16816(c[i], A, qf.x, qf.y);
-                mma16816(d[i], A, qf.z, qf.w);
+            e0[i] = lut_pair(lut, w[i], 2 * kk, l8);
+            e1[i] = lut_pair(lut, w[i], 2 * kk + 1, l8);
+            const uint32_t A[4] = {e0[i].x, e0[i].y, e1[i].x, e1[i].y};
+            if constexpr (G == 4) mma16816(c[i], A, bq[kk][0], bq[kk][1]);
+            else                  mma16816(c[i], A, qf.x, qf.y);
+        }
+        if constexpr (G == 8) {
+#pragma unroll
+            for (int rt = 0; rt < 2; ++rt) {
+                const uint32_t A[4] = {e0[2 * rt].x, e0[2 * rt + 1].x, e1[2 * rt].x, e1[2 * rt + 1].x};
+                mma16816(d[rt], A, qf.z, qf.w);
             }
         }
     }
 #pragma unroll
     for (int rt = 0; rt < 2; ++rt) {
         const float (&c0)[4] = c[2 * rt], (&c1)[4] = c[2 * rt + 1];
-        const float (&d0)[4] = d[2 * rt], (&d1)[4] = d[2 * rt + 1];
         out[rt][0] = c0[0] + c0[2];
         out[rt][1] = c0[1] + c0[3];
         out[rt][2] = c1[0] + c1[2];
         out[rt][3] = c1[1] + c1[3];
-        outl[rt][0] = d0[0] + d0[2];
-        outl[rt][1] = d0[1] + d0[3];
-        outl[rt][2] = d1[0] + d1[2];
-        outl[rt][3] = d1[1] + d1[3];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) outl[rt][i] = d[rt][i];
     }
 }
 
