@@ -731,13 +731,15 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     // per half-warp lane; the barrier after the q staging below orders it
     // before any use
     if constexpr (KMODE == 3 || KMODE == 4) {
+        // one (entry, two copies) per step: a 16-byte store of the entry twice
         constexpr int NE = KMODE == 3 ? kLut3Entries : kLut4Entries;
-        for (int i = threadIdx.x; i < NE; i += blockDim.x) {
-            const int e = i >> 4;
+        for (int i = threadIdx.x; i < NE / 2; i += blockDim.x) {
+            const int e = i >> 3;
             float h0, l0, h1, l1;
             split_f16(a.centroids[e & ((1 << KMODE) - 1)], h0, l0);
             split_f16(a.centroids[e >> KMODE], h1, l1);
-            key_lut[i] = make_uint2(pack_half2(h0, h1), pack_half2(l0, l1));
+            const uint32_t x = pack_half2(h0, h1), y = pack_half2(l0, l1);
+            reinterpret_cast<uint4*>(key_lut)[i] = make_uint4(x, y, x, y);
         }
     }
 
