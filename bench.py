@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -212,11 +213,15 @@ def _peaks():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the decode kernels' sources (both stages, both stage-1 paths)."""
+    """Hash of the decode kernels' code (both stages, both stage-1 paths):
+    the sources with their // comments removed and whitespace runs folded,
+    so that an edit of a comment keeps a recorded measurement valid."""
     h = hashlib.sha256()
     for f in ("tq_decode.cu", "tq_decode_mma.cu", "tq_decode_mma.cuh", "tq_decode_mma_sparse.cu",
               "tq_internal.h", "tq_device.cuh"):
-        h.update(open(os.path.join(ROOT, "quantized_kv_cache_04_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "quantized_kv_cache_04_gb300", "csrc", f), encoding="utf-8").read()
+        code = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -21,8 +21,8 @@
 // part).  FP8 keys and integer value codes are exact in fp16.  The value
 // path uses P' = p * v_scale and adds sum_t p_t v_zero_t separately
 // (v_hat = code * scale + zero).
-// Centroid lookups: 3-bit keys read code pairs from a shared-memory table
-// (one 8-byte load per pair: both centroids, hi and lo); 2- and 4-bit keys
+// Centroid lookups: 3- and 4-bit keys read code pairs from a shared-memory
+// table (one 8-byte load per pair: both centroids, hi and lo); 2-bit keys
 // select bytes of register tables with PRMT.
 //
 // Launch chain: stage 1 is a programmatic dependent of the previous kernel
