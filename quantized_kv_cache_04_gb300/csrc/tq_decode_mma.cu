@@ -100,19 +100,19 @@ MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len)
     const int stage = kTile * (m.smem_row + m.meta_bytes);
     // ring budget: two CTAs of 8 kv-head warps, or four CTAs of 4 warps, per
     // SM (about 16 warps); fewer kv heads take a proportional share (at
-    // least 28 KB), so that CTAs of 2 or 4 warps still fill an SM.  MSE keys
-    // with G = 8 also keep 4 KB of q fragments per warp, and 3- and 4-bit
-    // keys hold their pair table (8 / 32 KB) in static shared memory
-    const int qsm = (!L.key_fp8 && G > 4) ? m.hpc * 4096 : 0;
+    // least 28 KB), so that CTAs of 2 or 4 warps still fill an SM.  3- and
+    // 4-bit keys hold their pair table (8 / 32 KB) in static shared memory;
+    // MSE keys with G = 8 keep their q fragments in tensor memory
     m.static_smem = L.key_fp8 ? 0 : L.key_bits == 3 ? size_t(kLut3Entries) * 8
                                    : L.key_bits == 4 ? size_t(kLut4Entries) * 8 : 0;
     const int budget = m.hpc < Hk ? 56 * 1024 : (Hk >= 8 ? 100 * 1024 : std::max(28 * 1024, 100 * 1024 * Hk / 8));
-    int nst = (budget + (qsm ? 12 * 1024 : 0) - qsm - int(m.static_smem)) / stage;
+    int nst = (budget - int(m.static_smem)) / stage;
     nst = nst < 2 ? 2 : (nst > 6 ? 6 : nst);
     // the q staging at kernel start borrows the ring: hpc * (4 or 8) heads * 512 B
     while (nst * stage < m.hpc * (G <= 4 ? 4 : 8) * kHeadDim * 4) ++nst;
     m.nstages = nst;
-    m.smem = size_t(nst) * stage + 16 * size_t(nst) + size_t(qsm);   // ring, mbarrier + counter per stage, q
+    // ring, mbarrier + counter per stage, the tensor-memory address
+    m.smem = size_t(nst) * stage + 16 * size_t(nst) + 16;
     return m;
 }
 
@@ -126,6 +126,24 @@ int slots_t(const MmaGeom& m, bool soa, int num_sms)
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 32 * m.hpc, m.smem) != cudaSuccess)
         return 0;
+    if constexpr (KMODE != 8 && G == 8) {
+        // The instantiations that allocate tensor memory (32-128 of an SM's
+        // 512 columns per CTA) are reported at one CTA per SM, but run as
+        // many as registers and shared memory allow (two of 8 warps with 3-bit
+        // keys: one wave of 296 CTAs at batch 8 takes one wave's time)
+        cudaFuncAttributes at;
+        int dev = 0, smem_sm = 0, reserved = 0;
+        if (cudaFuncGetAttributes(&at, k) == cudaSuccess && at.numRegs > 0 && cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess) {
+            const int regs = (at.numRegs + 7) / 8 * 8;
+            const int by_regs = 65536 / (regs * 32 * m.hpc);
+            const int by_smem = int(size_t(smem_sm) / (m.smem + at.sharedSizeBytes + size_t(reserved)));
+            const int by_warps = 64 / m.hpc;
+            per_sm = std::max(per_sm, std::min(std::min(by_regs, by_smem), by_warps));
+        }
+        cudaGetLastError();
+    }
     return per_sm * num_sms;
 }
 

@@ -155,6 +155,53 @@ __device__ __forceinline__ void fence_async_shared()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Tensor memory (TMEM): a CTA's allocation is 128 lanes x ncols columns of
+// 32-bit cells; warp w reaches lanes 32 (w mod 4) .. 32 (w mod 4) + 31, one
+// per thread, at the address (lane << 16) + column.  Allocation and
+// deallocation are per warp (all lanes); the allocated address is written to
+// shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Four consecutive columns of this thread's lane (all lanes of the warp).
+// TMEM is not memory the compiler tracks: these carry no memory clobber, so
+// shared-memory loads may move across them; the volatile statements keep
+// their order among themselves (and with the MMAs that use the registers).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint4& v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;");
+}
+// the registers are valid after tmem_wait_ld()
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint4& v)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;");
+}
+
 // n little-endian 32-bit words starting at the 2-byte aligned shared address p.
 // `mis` (0 or 2, uniform per warp) is p mod 4.  MIS = 0 or 2 fixes it at
 // compile time (the tile loop is instantiated per warp misalignment: a
@@ -286,12 +333,12 @@ __device__ __forceinline__ void cvt_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& h
 // Scores of one 16-row MMA tile for the thread's rows (r0: row gid, r1:
 // row gid+8), FP8 or 2-bit keys.  Returns the raw accumulators: G = 4 -> sc
 // (cols head x {hi,lo}); G = 8 -> sc (q hi), scl (q lo).  2-bit keys with
-// G = 8 read their q fragments from shared memory (qsm: this lane's uint4 of
-// k-step 0, stride 32).
+// G = 8 read their q fragments from tensor memory (tq: this thread's columns
+// of k-step 0, four per k-step: q hi and q lo words).
 template <int KMODE, int G, bool KGEN, int KM, int NT>
 __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, int tig, int kmis,
                                         const uint32_t (&bq)[8][2], const uint32_t (&bql)[8][2],
-                                        const uint4* qsm, const uint32_t (&T)[NT][2], const uint2* lut,
+                                        uint32_t tq, const uint32_t (&T)[NT][2], const uint2* lut,
                                         uint32_t l8, float (&out)[4], float (&outl)[4])
 {
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -357,7 +404,9 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
                     mma16816(sc[kk & 1], Ahi, bq[kk][0], bq[kk][1]);
                 }
             } else {
-                const uint4 qf = qsm[32 * kk];      // q hi (x, y) and lo (z, w) of this k-step
+                uint4 qf;                           // q hi (x, y) and lo (z, w) of this k-step
+                tmem_ld4(tq + 4 * kk, qf);
+                tmem_wait_ld();
                 mma16816(sc[kk & 1], Ahi, qf.x, qf.y);
                 mma16816(scl[0], Ahi, qf.z, qf.w);
                 if constexpr (use_lo) mma16816(scl[1], Alo, qf.x, qf.y);
@@ -385,7 +434,7 @@ __device__ __forceinline__ void qk_tile(const uint8_t* r0, const uint8_t* r1, in
 // columns 2 tig / 2 tig + 1; [2] / [3] = token gid + 8.
 template <int KB, int G, int KM>
 __device__ __forceinline__ void qk_pairs(const uint8_t* const (&r)[4], int tig, int kmis,
-                                         const uint32_t (&bq)[8][2], const uint4* qsm, const uint2* lut,
+                                         const uint32_t (&bq)[8][2], uint32_t tq, const uint2* lut,
                                          uint32_t l8, float (&out)[2][4], float (&outl)[2][4])
 {
     uint32_t w[4][KB];
@@ -395,10 +444,15 @@ __device__ __forceinline__ void qk_pairs(const uint8_t* const (&r)[4], int tig, 
     // the 16 tokens of a row tile (rows = tokens gid, gid + 8); the term it
     // leaves out, k lo . q lo, is below 2^-22 of |k| |q|
     float c[4][4] = {}, d[2][4] = {};
+    // G = 8: q fragments of k-step kk + 1 are read from tensor memory while
+    // k-step kk runs
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         uint4 qf;
-        if constexpr (G == 8) qf = qsm[32 * kk];
+        if constexpr (G == 8) {
+            tmem_ld4(tq + 4 * kk, qf);
+            tmem_wait_ld();
+        }
         uint2 e0[4], e1[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -622,13 +676,29 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     int* done = reinterpret_cast<int*>(full + NST);
     int* bad_pages = done + NST;               // a block-table entry outside the cache was met
     int* finished = bad_pages + 1;             // warps past their epilogue
+    // MSE keys with G = 8 keep their q fragments (hi and lo, 32 words per
+    // thread) in tensor memory: 32 columns per group of 4 warps, the address
+    // written by the allocation to the word after the stage counters
+    constexpr bool kQt = KMODE != 8 && G == 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + NST * stage_bytes + 16 * NST);
+    const uint32_t q_cols = nwarps <= 4 ? 32u : nwarps <= 8 ? 64u : 128u;
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) { mbar_init(&full[i], 1); done[i] = 0; }
         *bad_pages = 0;
         *finished = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if constexpr (kQt) {
+        if (warp == 0) tmem_alloc(tmem_slot, q_cols);
+        tmem_fence_before_sync();
+    }
     __syncthreads();
+    uint32_t tq = 0;                           // this thread's q columns (k-step 0)
+    if constexpr (kQt) {
+        tmem_fence_after_sync();
+        tq = *reinterpret_cast<volatile uint32_t*>(tmem_slot) + ((32u * uint32_t(warp & 3)) << 16) +
+             32u * uint32_t(warp >> 2);
+    }
     // Only rows of tokens < L are copied: block-table entries past the
     // sequence's last page are never read.  Skipped rows keep stale bytes and
     // are masked out of the softmax.
@@ -743,11 +813,10 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         }
     }
 
-    // MSE keys with G = 8 keep their q fragments in shared memory after the
-    // ring's barriers (4 KB per warp, read once per k-step) instead of 32
-    // registers: the register file is the limit of that instantiation.
-    constexpr bool kQsm = KMODE != 8 && G == 8;
-    uint4* qsm = reinterpret_cast<uint4*>(smem + NST * stage_bytes + 16 * NST) + warp * 256 + lane;
+    // MSE keys with G = 8 keep their q fragments in tensor memory (read once
+    // per k-step) instead of 32 registers (the register file is the limit of
+    // that instantiation) or 4 KB of shared memory per warp (which a third
+    // ring stage needs).
     uint32_t bq[8][2], bql[8][2];
     {
         float* sq = reinterpret_cast<float*>(smem + q_base) + warp * G * kHeadDim;
@@ -799,12 +868,13 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
                 bq[kk][1] = pack_half2(hi[2], hi[3]);
                 bql[kk][0] = pack_half2(lo[0], lo[1]);
                 bql[kk][1] = pack_half2(lo[2], lo[3]);
-                if constexpr (kQsm) {
-                    qsm[32 * kk] = make_uint4(bq[kk][0], bq[kk][1], bql[kk][0], bql[kk][1]);
+                if constexpr (kQt) {
+                    tmem_st4(tq + 4 * kk, make_uint4(bq[kk][0], bq[kk][1], bql[kk][0], bql[kk][1]));
                     bq[kk][0] = bq[kk][1] = bql[kk][0] = bql[kk][1] = 0u;
                 }
             }
         }
+        if constexpr (kQt) tmem_wait_st();
         __syncthreads();            // every warp is done with the staging area
     }
     if (warp == 0)
@@ -856,7 +926,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     auto tile = [&](const uint8_t* st, const uint8_t* sm, int t0, auto partial_tag, auto lo_tag,
                     auto km_tag, auto vm_tag) {
         constexpr bool PARTIAL = decltype(partial_tag)::value;
-        constexpr bool KGEN = decltype(lo_tag)::value;
+        [[maybe_unused]] constexpr bool KGEN = decltype(lo_tag)::value;
         constexpr int KM = decltype(km_tag)::value, VM = decltype(vm_tag)::value;
         // ---- scores of both 16-row tiles
         float s[NH][2][2], vs[2][2], vz[2][2];
@@ -865,12 +935,12 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
         if constexpr (KMODE == 3 || KMODE == 4) {
             const uint8_t* const rr[4] = {st + tau0 * rs, st + tau1 * rs, st + (16 + tau0) * rs,
                                           st + (16 + tau1) * rs};
-            qk_pairs<KMODE, G, KM>(rr, tig, kmis, bq, qsm, key_lut, l8, sc2, scl2);
+            qk_pairs<KMODE, G, KM>(rr, tig, kmis, bq, tq, key_lut, l8, sc2, scl2);
         }
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt) {
-            const uint8_t* r0 = st + (16 * rt + tau0) * rs;
-            const uint8_t* r1 = st + (16 * rt + tau1) * rs;
+            [[maybe_unused]] const uint8_t* r0 = st + (16 * rt + tau0) * rs;
+            [[maybe_unused]] const uint8_t* r1 = st + (16 * rt + tau1) * rs;
             const uint8_t* m0 = sm + (16 * rt + tau0) * mrs;
             const uint8_t* m1 = sm + (16 * rt + tau1) * mrs;
             float sc[4], scl[4];
@@ -878,7 +948,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) { sc[i] = sc2[rt][i]; scl[i] = scl2[rt][i]; }
             } else {
-                qk_tile<KMODE, G, KGEN, KM>(r0, r1, tig, kmis, bq, bql, qsm, T, key_lut, l8, sc, scl);
+                qk_tile<KMODE, G, KGEN, KM>(r0, r1, tig, kmis, bq, bql, tq, T, key_lut, l8, sc, scl);
             }
             float n0 = 1.f, n1 = 1.f;
             if constexpr (KMODE != 8) { n0 = lds_f16(m0 + a.g.m_norm); n1 = lds_f16(m1 + a.g.m_norm); }
@@ -1066,38 +1136,47 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             a.mid[(((long long)b * Hq + h * Gall + qh0 + lane) * S + split) * (kHeadDim + 1) + kHeadDim] =
                 __int_as_float(0x7fc00000);
         finish();
-        return;
+    } else {
+        // ---------------- epilogue: finish the row sums, write o_s and lse_s.
+        // The value accumulators hold 2^-9 of sum_t p_t v_scale_t code_t.
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+#pragma unroll
+            for (int m = 4; m < 32; m <<= 1) {
+                l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], m);
+                z_run[j] += __shfl_xor_sync(0xffffffffu, z_run[j], m);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+            const int g = G == 4 ? tig : 2 * tig + j;
+            if (g >= Greal) continue;
+            const int hq = h * Gall + qh0 + g;
+            float* mp = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
+            const float inv = 1.f / l_run[j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d = 16 * gid + 2 * i;
+                float e, o;
+                if constexpr (G == 4) { e = acc[i][0] + acc[i][1]; o = acc[i][2] + acc[i][3]; }
+                else { e = j == 0 ? acc[i][0] : acc[i][1]; o = j == 0 ? acc[i][2] : acc[i][3]; }
+                mp[d] = (e * 512.f + z_run[j]) * inv;
+                mp[d + 1] = (o * 512.f + z_run[j]) * inv;
+            }
+            if (gid == 0) mp[kHeadDim] = (m_run[j] + log2f(l_run[j])) * 0.6931471805599453f;
+        }
+        finish();
     }
-
-    // ---------------- epilogue: finish the row sums, write o_s and lse_s.
-    // The value accumulators hold 2^-9 of sum_t p_t v_scale_t code_t.
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-#pragma unroll
-        for (int m = 4; m < 32; m <<= 1) {
-            l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], m);
-            z_run[j] += __shfl_xor_sync(0xffffffffu, z_run[j], m);
+    // every warp of the CTA is done with its q columns: free them (the
+    // allocating warp; all warps reach this point, the waits being bounded)
+    if constexpr (kQt) {
+        tmem_fence_before_sync();
+        __syncthreads();
+        if (warp == 0) {
+            tmem_fence_after_sync();
+            tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), q_cols);
         }
     }
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-        const int g = G == 4 ? tig : 2 * tig + j;
-        if (g >= Greal) continue;
-        const int hq = h * Gall + qh0 + g;
-        float* mp = a.mid + (((long long)b * Hq + hq) * S + split) * (kHeadDim + 1);
-        const float inv = 1.f / l_run[j];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int d = 16 * gid + 2 * i;
-            float e, o;
-            if constexpr (G == 4) { e = acc[i][0] + acc[i][1]; o = acc[i][2] + acc[i][3]; }
-            else { e = j == 0 ? acc[i][0] : acc[i][1]; o = j == 0 ? acc[i][2] : acc[i][3]; }
-            mp[d] = (e * 512.f + z_run[j]) * inv;
-            mp[d + 1] = (o * 512.f + z_run[j]) * inv;
-        }
-        if (gid == 0) mp[kHeadDim] = (m_run[j] + log2f(l_run[j])) * 0.6931471805599453f;
-    }
-    finish();
 }
 
 template <typename TQ, int KMODE, int VBITS, int G, bool SPARSE>

@@ -51,10 +51,13 @@ def _stuck(p, tile, polls):
     return out.cpu().numpy(), lse.cpu().numpy()
 
 
-@pytest.mark.parametrize("preset", ["turboquant_k8v4", "turboquant_k3v4_nc"])
-def test_bounded_wait_runs_out_and_marks_the_split(preset):
+@pytest.mark.parametrize("preset,q_heads", [("turboquant_k8v4", 32), ("turboquant_k3v4_nc", 32),
+                                            ("turboquant_k3v4_nc", 64)])
+def test_bounded_wait_runs_out_and_marks_the_split(preset, q_heads):
+    """Groups of 4 and of 8 query heads; with 8 and Lloyd-Max keys the CTA
+    also frees its tensor-memory q columns on the way out."""
     import bench
-    w = wl.make("sweep", preset=preset, ctx=2048, batch=3)
+    w = wl.make("sweep", preset=preset, ctx=2048, batch=3, q_heads=q_heads)
     p = bench.Problem(w, torch.device("cuda"), 2)         # 2 splits of 32 tiles
     assert tq.tq_decode_kernel_kind(p.c.preset, 128, w.Hq, w.Hk) == 1
     o0, l0 = _clean(p)
