@@ -376,11 +376,10 @@ int v1_slots(int G, int num_sms)
 }
 
 // (CTAs per split, resident CTA slots) of the stage-1 kernel for a shape,
-// cached per device (and per CTA width: whole rows or 4 kv heads).
-void stage1_shape(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len, int* cps, int* slots)
+// cached per device.
+void stage1_shape(const tq_layout& L, bool soa, int Hk, int G, int* cps, int* slots)
 {
-    struct Entry { int dev, kf8, kb, vb, soa, hk, g, rows, cps, slots; };
-    const int rows = max_seq_len >= kFullRowsFrom ? 1 : 0;
+    struct Entry { int dev, kf8, kb, vb, soa, hk, g, cps, slots; };
     static std::mutex mu;
     static std::vector<Entry> cache;
     int dev = -1, num_sms = 0;
@@ -394,7 +393,7 @@ void stage1_shape(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len, 
         std::lock_guard<std::mutex> lock(mu);
         for (const Entry& e : cache)
             if (e.dev == dev && e.kf8 == L.key_fp8 && e.kb == L.key_bits && e.vb == L.value_bits &&
-                e.soa == int(soa) && e.hk == Hk && e.g == G && e.rows == rows) {
+                e.soa == int(soa) && e.hk == Hk && e.g == G) {
                 *cps = e.cps;
                 *slots = e.slots;
                 return;
@@ -402,7 +401,7 @@ void stage1_shape(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len, 
     }
     int c = Hk, n = 0;
     if (mma_stage1_supported(L, soa, Hk, G)) {
-        mma_stage1_shape(L, soa, Hk, G, max_seq_len, num_sms, &c, &n);
+        mma_stage1_shape(L, soa, Hk, G, num_sms, &c, &n);
     } else if (num_sms > 0) {
         c = Hk;                    // grid (splits, kv heads, batch)
         if (L.key_fp8) n = v1_slots<true, 4, 4>(G, num_sms);
@@ -416,7 +415,7 @@ void stage1_shape(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len, 
         n = 2 * kNumSMs;           // no device to ask: two CTAs per SM of a GB300
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (cache.size() < 256) cache.push_back({dev, L.key_fp8, L.key_bits, L.value_bits, int(soa), Hk, G, rows, c, n});
+    if (cache.size() < 256) cache.push_back({dev, L.key_fp8, L.key_bits, L.value_bits, int(soa), Hk, G, c, n});
     *cps = c;
     *slots = n;
 }
@@ -427,7 +426,7 @@ int pick_splits(const tq_layout& L, bool soa, int batch, int num_q_heads, int nu
 {
     if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_seq_len <= 0) return 1;
     int cps = 1, slots = 1;
-    stage1_shape(L, soa, num_kv_heads, num_q_heads / num_kv_heads, max_seq_len, &cps, &slots);
+    stage1_shape(L, soa, num_kv_heads, num_q_heads / num_kv_heads, &cps, &slots);
     // Critical path of stage 1 in 32-token tiles: the CTAs of all splits run
     // in ceil(CTAs / slots) waves, each as long as one split's tiles plus a
     // fixed start-up (q preparation, first copy latency, epilogue) worth about
@@ -513,7 +512,7 @@ int decode_impl(int preset, int head_dim, int batch, int num_q_heads, int num_kv
     if (mma) {
         rc = launch_mma_stage1(L, soa, q_dtype, query, kv_cache, num_blocks, block_table, block_table_stride, seq_lens,
                                softmax_scale, S, signs, centroids, a.mid, batch, num_q_heads,
-                               num_kv_heads, block_size, v_threshold, max_seq_len, st, stuck_tile,
+                               num_kv_heads, block_size, v_threshold, st, stuck_tile,
                                wait_polls);
         if (rc) return rc;
     } else {

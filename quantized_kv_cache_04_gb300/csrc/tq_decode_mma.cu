@@ -5,6 +5,8 @@
 #include <algorithm>
 #include <array>
 #include <cmath>
+#include <cstdint>
+#include <cstring>
 
 namespace tq {
 
@@ -70,6 +72,43 @@ float two_bit_alpha()
     return alpha;
 }
 
+// cuTensorMapEncodeTiled, through the runtime's driver entry point (no link
+// against the driver library); null when unavailable.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled()
+{
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return EncodeTiledFn(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The cache as `rows` rows of row_bytes (32-bit words), boxes of box_bytes x
+// box_rows.  False when the map cannot be encoded.
+bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, int row_bytes, int box_bytes,
+                     int box_rows)
+{
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(row_bytes / 4), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+    const cuuint32_t box[2] = {cuuint32_t(box_bytes / 4), cuuint32_t(box_rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Launch geometry shared by the launcher and the occupancy query.
 struct MmaGeom {
     int hpc, copy_bytes, smem_row, meta_bytes, nstages;
@@ -77,19 +116,16 @@ struct MmaGeom {
     size_t static_smem;   // the kernel's own: the 3- or 4-bit keys' pair table
 };
 
-MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G, int max_seq_len)
+MmaGeom mma_geom(const tq_layout& L, bool soa, int Hk, int G)
 {
     MmaGeom m;
     const SlotGeom g = geom_of(L, soa);
     const int rec = soa ? g.data_bytes : L.slot_size_aligned;   // data bytes per (token, head)
     // FP8-key rows split into CTAs of 4 kv heads (4 records are a whole number
     // of 16-byte copy units): half-size CTAs, four per SM, each waiting on
-    // only 4 warps before a stage is refilled.  With 8 kv heads and long
-    // contexts, CTAs of whole rows copy a page segment at once, which pays
-    // more (32K: 0.334 -> 0.302 ms, 128K: 0.319 -> 0.297 ms; 8K: 0.088 ->
-    // 0.089 ms, A/B on one GB300).
-    const bool full_rows = Hk <= 8 && max_seq_len >= kFullRowsFrom;
-    m.hpc = (L.key_fp8 && Hk % 4 == 0 && Hk > 4 && !full_rows && (4 * rec) % 16 == 0 &&
+    // only 4 warps before a stage is refilled; AoS rows arrive by one tensor
+    // copy per page segment (the launcher's map)
+    m.hpc = (L.key_fp8 && Hk % 4 == 0 && Hk > 4 && (4 * rec) % 16 == 0 &&
              (!soa || (4 * g.meta_bytes) % 16 == 0))
                 ? 4 : Hk;
     m.copy_bytes = m.hpc * rec;
@@ -156,10 +192,8 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
                                          (L.key_bits == 2 && L.value_bits == 2)));
     const bool vals_ok = L.value_bits >= 2 && L.value_bits <= 4;
     if (!keys_ok || !vals_ok || num_kv_heads < 1 || group < 1 || group > kMaxGroup) return false;
-    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group, 0);
+    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
     const int row = m.copy_bytes;
-    // (the whole-row CTAs that FP8 keys with 8 kv heads take at long
-    // contexts copy 1568-byte rows: whole 16-byte units too)
     // Copies are 16-byte units: rows of a multiple of 16 bytes are copied
     // one by one (or per page segment); an AoS CTA that takes whole rows of
     // a multiple of 4 bytes copies whole page segments (16 or 32 rows: a
@@ -170,10 +204,10 @@ bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int gr
            2 * kTile * (row + 16 + m.meta_bytes) <= 110 * 1024;
 }
 
-void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int max_seq_len,
-                      int num_sms, int* ctas_per_split, int* slots)
+void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int num_sms,
+                      int* ctas_per_split, int* slots)
 {
-    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group, max_seq_len);
+    const MmaGeom m = mma_geom(L, soa, num_kv_heads, group);
     *ctas_per_split = num_kv_heads / m.hpc * (group > 4 ? (group + 7) / 8 : 1);
     int n = 0;
     if (num_sms > 0) {
@@ -197,7 +231,7 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
                       long long num_blocks, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
-                      float v_threshold, int max_seq_len, cudaStream_t st, int stuck_tile,
+                      float v_threshold, cudaStream_t st, int stuck_tile,
                       uint32_t wait_polls)
 {
     MmaArgs a;
@@ -222,12 +256,24 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
     a.bs = bs;
     a.bs_log2 = bs == 16 ? 4 : bs == 32 ? 5 : bs == 64 ? 6 : 7;
     a.row_bytes = Hk * L.slot_size_aligned;
-    const MmaGeom m = mma_geom(L, soa, Hk, a.G, max_seq_len);
+    const MmaGeom m = mma_geom(L, soa, Hk, a.G);
     a.hpc = m.hpc;
     // groups above 8: CTAs of 8 query heads per kv head, each reading the
     // kv heads' rows (neighbouring CTAs: the second read mostly hits L2)
     a.nqg = a.G > 4 ? (a.G + 7) / 8 : 1;
     a.copy_bytes = m.copy_bytes;
+    // CTAs of part of each AoS row (FP8 keys, 4 kv heads): a page segment's
+    // parts by one tensor copy instead of one bulk copy per row, when the
+    // rows land unpadded (784-byte parts: 16 mod 32) and the map's limits
+    // hold (16-byte aligned cache and row stride, at most 256 words per box
+    // row, rows addressable as int)
+    a.use_tmap = 0;
+    std::memset(&a.tmap, 0, sizeof(a.tmap));
+    const int seg_rows = bs < kTile ? bs : kTile;
+    if (!soa && m.hpc < Hk && m.smem_row == m.copy_bytes && m.copy_bytes % 16 == 0 && m.copy_bytes / 4 <= 256 &&
+        a.row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(kv_cache) & 15) == 0 && num_blocks > 0 &&
+        num_blocks * bs <= 0x7fffffffLL)
+        a.use_tmap = encode_rows_map(&a.tmap, kv_cache, num_blocks * bs, a.row_bytes, m.copy_bytes, seg_rows) ? 1 : 0;
     a.smem_row = m.smem_row;
     a.meta_bytes = m.meta_bytes;
     a.nstages = m.nstages;

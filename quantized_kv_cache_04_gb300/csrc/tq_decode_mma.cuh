@@ -37,12 +37,19 @@
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
+#include <cuda.h>
+
 #include <cmath>
 #include <type_traits>
 
 namespace tq {
 
 struct MmaArgs {
+    // CTAs that take part of each token row (FP8 keys, 4 of 8+ kv heads):
+    // a 2-D map of the cache as rows of 32-bit words (inner: the row, outer:
+    // block * bs + offset), boxes of the CTA's copy_bytes x one page segment
+    CUtensorMap tmap;
+    int use_tmap;            // 1: page segments by tensor copies through tmap
     const void* query;
     const uint8_t* cache;
     long long num_blocks;    // block-table entries outside [0, num_blocks) are caller errors
@@ -148,6 +155,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// One box of a 2-D tensor map (x: 32-bit words within a row, y: row) into
+// shared memory, completing on the mbarrier.  x * 4 is a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
 __device__ __forceinline__ void fence_async_shared()
@@ -610,9 +626,9 @@ __device__ __forceinline__ void pv_tile(const uint8_t* tile_v, int rs, int gid, 
 // One CTA = (split, sequence); warp w = kv head w; each iteration consumes a
 // 32-token tile (two 16-row MMA tiles) with one softmax update.
 template <typename TQ, int KMODE, int VBITS, int G, bool SOA, bool SPARSE>
-__global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
+__global__ void __launch_bounds__(512) stage1_mma_kernel(const __grid_constant__ MmaArgs a)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     // 3-bit keys: the code-pair centroid table (8 KB; one element elsewhere)
     __shared__ __align__(16) uint2 key_lut[KMODE == 3 ? kLut3Entries : KMODE == 4 ? kLut4Entries : 1];
     // launched as a programmatic dependent of the previous kernel in the
@@ -709,16 +725,21 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
     const long long hs_g = soa ? a.g.data_bytes : a.g.slot;    // head stride in a global data row
     const long long drow = soa ? (long long)a.Hk * a.g.data_bytes : row_bytes;
     bool bad_seen = false;                     // this lane replaced a page outside the cache
+    // tensor copies land on 128-byte aligned stage and segment offsets
+    // (stage_bytes and the segment size are multiples of 128 for these
+    // rows); a ring base that is not would take the per-row copies
+    const bool use_tm = a.use_tmap && !soa && (smem_u32(smem) & 127u) == 0;
     auto issue = [&](int tile, int stage) {   // called by all lanes of one warp
         if (tile >= ntiles) return;
         uint8_t* dst = smem + stage * stage_bytes;
         uint64_t* bar = &full[stage];
         const int tbase = t_begin + tile * kTile;
         // data rows: one copy per page segment when the CTA takes whole rows
-        // and the shared stride equals the global one, else one per row;
-        // SoA metadata rows (unpadded in shared memory): one copy per page
-        // segment when the CTA takes every kv head
-        const bool seg_d = rs == drow && cb == drow;
+        // and the shared stride equals the global one, or through the tensor
+        // map (a box of the CTA's part of a segment's rows), else one per
+        // row; SoA metadata rows (unpadded in shared memory): one copy per
+        // page segment when the CTA takes every kv head
+        const bool seg_d = (rs == drow && cb == drow) || use_tm;
         const bool seg_m = soa && mb == a.Hk * a.g.meta_bytes;
         const int len_d = seg_d ? seg_rows : 1, len_m = seg_m ? seg_rows : 1;   // rows per copy
         const int nd = min(kTile / len_d, (L - tbase + len_d - 1) / len_d);
@@ -742,8 +763,13 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(MmaArgs a)
             if ((unsigned long long)page >= (unsigned long long)a.num_blocks) { page = 0; bad_seen = true; }
             const int off = t & ((1 << lg) - 1);
             const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
-            const uint8_t* src = soa ? blk + off * drow + h0 * hs_g : blk + off * (long long)row_bytes + h0 * hs_g;
-            bulk_g2s(dst + lane * len_d * rs, src, uint32_t(len_d * cb), bar);
+            if (use_tm) {
+                tma_load_2d(dst + lane * len_d * rs, &a.tmap, int(h0 * hs_g) >> 2, int((page << lg) + off), bar);
+            } else {
+                const uint8_t* src =
+                    soa ? blk + off * drow + h0 * hs_g : blk + off * (long long)row_bytes + h0 * hs_g;
+                bulk_g2s(dst + lane * len_d * rs, src, uint32_t(len_d * cb), bar);
+            }
             if (soa && same) {
                 const uint8_t* meta = blk + (1LL << lg) * drow + ((long long)off * a.Hk + h0) * a.g.meta_bytes;
                 bulk_g2s(dst + kTile * rs + lane * len_m * mb, meta, uint32_t(len_m * mb), bar);

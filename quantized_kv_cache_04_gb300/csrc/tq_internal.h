@@ -92,13 +92,10 @@ __device__ __forceinline__ void slot_ptrs(const SlotGeom& g, const uint8_t* cach
 
 // Tensor-core stage 1 (tq_decode_mma.cu): which shapes it serves, and its launcher.
 bool mma_stage1_supported(const tq_layout& L, bool soa, int num_kv_heads, int group);
-// FP8 keys with 8 kv heads take CTAs of whole token rows (one copy per page
-// segment) from this context length on, CTAs of 4 kv heads below it.
-constexpr int kFullRowsFrom = 16384;
 // CTAs one split of one sequence launches, and resident CTA slots on num_sms
 // SMs (0 when the occupancy query fails, e.g. without a device).
-void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int max_seq_len,
-                      int num_sms, int* ctas_per_split, int* slots);
+void mma_stage1_shape(const tq_layout& L, bool soa, int num_kv_heads, int group, int num_sms,
+                      int* ctas_per_split, int* slots);
 // Polls of a stage's mbarrier before stage 1 gives up on it (the split's
 // lse becomes NaN); each poll sleeps at most 20 us waiting for the phase,
 // so a stage that never completes is given up after about 1.3 s.  A test
@@ -108,7 +105,7 @@ int launch_mma_stage1(const tq_layout& L, bool soa, int q_dtype, const void* que
                       long long num_blocks, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       float softmax_scale, int num_splits, const int8_t* signs,
                       const float* centroids, float* mid, int B, int Hq, int Hk, int bs,
-                      float v_threshold, int max_seq_len, cudaStream_t st, int stuck_tile = -1,
+                      float v_threshold, cudaStream_t st, int stuck_tile = -1,
                       uint32_t wait_polls = kWaitPolls);
 
 }  // namespace tq

@@ -50,7 +50,7 @@ CASES = [  # (G, Hk, bs, seq_lens, splits): CUDA-core and tensor-core stage 1 sh
     (16, 8, 16, [200], 2),
     (2, 1, 32, [300, 45], 0),
     (4, 3, 16, [77, 400], 0),
-    (4, 8, 16, [16500, 200], 0),   # 16K+ tokens: FP8 keys take CTAs of whole rows
+    (4, 8, 16, [16500, 200], 0),   # a 16K-token sequence next to a short one
 ]
 
 
