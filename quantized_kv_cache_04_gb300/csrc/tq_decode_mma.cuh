@@ -635,13 +635,19 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(const __grid_constant__
     // stream (typically the store of the step's new tokens): wait for it to
     // complete before the first read of global memory
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int qg = blockIdx.x % a.nqg;        // which 8 query heads of each kv head (G > 8)
-    const int split = blockIdx.x / a.nqg;
+    // blockIdx.x = (split * nqg + qg) * (Hk / hpc) + kv-head group: the
+    // CTAs that read the parts of the same token rows (kv-head groups) and
+    // the same pages (query-head groups) are neighbours in launch order, so
+    // they run together (DRAM pages and L2 lines are used once)
+    const int ngroups = a.Hk / a.hpc;
+    const int kvg = blockIdx.x % ngroups;     // which hpc kv heads
+    const int qg = (blockIdx.x / ngroups) % a.nqg;   // which 8 query heads of each kv head (G > 8)
+    const int split = blockIdx.x / ngroups / a.nqg;
     const int b = a.lpt ? seq_of_rank(a.seq_lens, gridDim.y, blockIdx.y, reinterpret_cast<int*>(smem))
                         : blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const int h0 = blockIdx.z * a.hpc;        // first kv head of this CTA
+    const int h0 = kvg * a.hpc;               // first kv head of this CTA
     const int h = h0 + warp;                   // this warp's kv head
     // query heads of this CTA per kv head: Greal of them from qh0 (all G
     // when G <= 8); query head of (kv head hh, column g) = hh * Gall + qh0 + g
@@ -728,7 +734,8 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(const __grid_constant__
     // tensor copies land on 128-byte aligned stage and segment offsets
     // (stage_bytes and the segment size are multiples of 128 for these
     // rows); a ring base that is not would take the per-row copies
-    const bool use_tm = a.use_tmap && !soa && (smem_u32(smem) & 127u) == 0;
+    // (FP8 keys only: the other instantiations carry no tensor-copy code)
+    const bool use_tm = KMODE == 8 && !soa && a.use_tmap && (smem_u32(smem) & 127u) == 0;
     auto issue = [&](int tile, int stage) {   // called by all lanes of one warp
         if (tile >= ntiles) return;
         uint8_t* dst = smem + stage * stage_bytes;
@@ -749,7 +756,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(const __grid_constant__
             // the test hook's tile expects 16 bytes that no copy brings: its
             // stage never completes and the bounded waits run out
             const uint32_t extra =
-                (tile == a.stuck_tile && split == 0 && qg == 0 && b == 0 && blockIdx.z == 0) ? 16u : 0u;
+                (tile == a.stuck_tile && split == 0 && qg == 0 && b == 0 && kvg == 0) ? 16u : 0u;
             mbar_expect_tx(bar, uint32_t(nd * len_d * cb + nm * len_m * mb) + extra);
         }
         __syncwarp();
@@ -763,7 +770,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(const __grid_constant__
             if ((unsigned long long)page >= (unsigned long long)a.num_blocks) { page = 0; bad_seen = true; }
             const int off = t & ((1 << lg) - 1);
             const uint8_t* blk = a.cache + (page << lg) * (long long)row_bytes;
-            if (use_tm) {
+            if (KMODE == 8 && !soa && use_tm) {
                 tma_load_2d(dst + lane * len_d * rs, &a.tmap, int(h0 * hs_g) >> 2, int((page << lg) + off), bar);
             } else {
                 const uint8_t* src =
@@ -1213,7 +1220,7 @@ cudaError_t launch_t(const MmaArgs& a, int B, size_t smem, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_splits * a.nqg, B, a.Hk / a.hpc);   // a split's query-head groups side by side
+    cfg.gridDim = dim3(a.num_splits * a.nqg * (a.Hk / a.hpc), B, 1);   // see the kernel's blockIdx.x
     cfg.blockDim = dim3(32 * a.hpc);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
