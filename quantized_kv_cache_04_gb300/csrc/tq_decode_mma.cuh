@@ -691,6 +691,7 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(const __grid_constant__
     const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
     const int lg = a.bs_log2;
     const int seg_rows = kTile < (1 << lg) ? kTile : (1 << lg);   // rows per page segment
+    const int seg_lg = lg < 5 ? lg : 5;                                  // log2(seg_rows)
     // Per stage: `full` completes when the stage's bytes have landed; `done`
     // counts the warps finished with it.  The warp that finishes a stage last
     // refills it, so warps never wait on each other, only on data.
@@ -749,8 +750,9 @@ __global__ void __launch_bounds__(512) stage1_mma_kernel(const __grid_constant__
         const bool seg_d = (rs == drow && cb == drow) || use_tm;
         const bool seg_m = soa && mb == a.Hk * a.g.meta_bytes;
         const int len_d = seg_d ? seg_rows : 1, len_m = seg_m ? seg_rows : 1;   // rows per copy
-        const int nd = min(kTile / len_d, (L - tbase + len_d - 1) / len_d);
-        const int nm = soa ? min(kTile / len_m, (L - tbase + len_m - 1) / len_m) : 0;
+        const int lg_d = seg_d ? seg_lg : 0, lg_m = seg_m ? seg_lg : 0;      // (powers of two)
+        const int nd = min(kTile >> lg_d, (L - tbase + len_d - 1) >> lg_d);
+        const int nm = soa ? min(kTile >> lg_m, (L - tbase + len_m - 1) >> lg_m) : 0;
         if (lane == 0) {
             fence_async_shared();             // prior generic reads of this stage before the async writes
             // the test hook's tile expects 16 bytes that no copy brings: its
