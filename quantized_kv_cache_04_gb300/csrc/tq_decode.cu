@@ -134,12 +134,13 @@ __global__ void __launch_bounds__(kWarps * 32) stage1_kernel(DecodeArgs a)
     }
 
     const int32_t* bt = a.block_table + (long long)b * a.bt_stride;
+    const int lgbs = 31 - __clz(a.bs);       // block sizes are powers of two
     bool bad = false;
     for (int t = t0 + warp; t < t1; t += kWarps) {
-        const long long page = bt[t / a.bs];
+        const long long page = bt[t >> lgbs];
         if (page < 0 || page >= a.num_blocks) { bad = true; continue; }   // not read; the rows become NaN
         const uint8_t *sp, *mp;              // data and metadata of the record
-        slot_ptrs(a.g, a.cache, page, t % a.bs, h, a.bs, a.Hk, sp, mp);
+        slot_ptrs(a.g, a.cache, page, t & (a.bs - 1), h, a.bs, a.Hk, sp, mp);
 
         float kv[4];
         float knorm = 1.f;

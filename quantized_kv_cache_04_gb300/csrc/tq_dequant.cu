@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(32 * kDqWarps) dequant2_kernel(DqArgs a)
 #pragma unroll
     for (int i = 0; i < 8; ++i) sg[i] = KBITS > 0 ? float(a.signs[8 * l + i]) : 1.f;
     const int Hk = a.Hk;
+    const int lgbs = 31 - __clz(a.bs);
     const long long nw = (long long)gridDim.x * kDqWarps;
     for (long long n = (long long)blockIdx.x * kDqWarps + (threadIdx.x >> 5); n < a.num_tokens; n += nw) {
         const long long slot = a.slot_mapping[n];
@@ -151,8 +152,9 @@ __global__ void __launch_bounds__(32 * kDqWarps) dequant2_kernel(DqArgs a)
             }
             continue;
         }
-        const long long page = slot / a.bs;
-        const int off = int(slot - page * a.bs);
+        // (block sizes are powers of two: no division per token)
+        const long long page = slot >> lgbs;
+        const int off = int(slot & (a.bs - 1));
         for (int h0 = 0; h0 < Hk; h0 += 4) {
             const int ha = h0 + hw, hb = h0 + 2 + hw;      // this half-warp's two heads
             const bool la = ha < Hk, lb = hb < Hk;        // an odd count leaves halves idle

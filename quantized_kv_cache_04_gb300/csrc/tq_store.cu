@@ -236,23 +236,25 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreArgs a)
         // records from the staged slots
         {
             const int Hk = a.num_kv_heads, kd = a.g.key_data_bytes;
-            const long long page = slot_idx / a.bs;
-            const int off = int(slot_idx - page * a.bs);
+            const long long page = slot_idx >> (31 - __clz(a.bs));    // block sizes are powers of two
+            const int off = int(slot_idx & (a.bs - 1));
             uint8_t* blk = a.cache + page * a.bs * (long long)row_bytes;
             uint16_t* dd = reinterpret_cast<uint16_t*>(blk + (long long)off * Hk * a.g.data_bytes);
             uint16_t* md = reinterpret_cast<uint16_t*>(blk + (long long)a.bs * Hk * a.g.data_bytes +
                                                        (long long)off * Hk * a.g.meta_bytes);
+            // warp hh moves head hh's records (one warp per kv head)
             const int dh = a.g.data_bytes / 2, mh = a.g.meta_bytes / 2;
-            for (int i = threadIdx.x; i < Hk * dh; i += blockDim.x) {
-                const int hh = i / dh, j = 2 * (i - hh * dh);
+            const int hh = threadIdx.x >> 5, ln = threadIdx.x & 31;
+            for (int i = ln; i < dh; i += 32) {
+                const int j = 2 * i;
                 const int src = hh * S + (j < kd ? j : a.g.off_v_data + (j - kd));
-                dd[i] = *reinterpret_cast<const uint16_t*>(row + src);
+                dd[hh * dh + i] = *reinterpret_cast<const uint16_t*>(row + src);
             }
-            for (int i = threadIdx.x; i < Hk * mh; i += blockDim.x) {
-                const int hh = i / mh, f = i - hh * mh;
+            if (ln < mh) {
+                const int f = ln;
                 const int fo = a.g.key_fp8 ? (f == 0 ? a.g.off_v_scale : a.g.off_v_zero)
                                            : (f == 0 ? a.g.off_k_norm : f == 1 ? a.g.off_v_scale : a.g.off_v_zero);
-                md[i] = *reinterpret_cast<const uint16_t*>(row + hh * S + fo);
+                md[hh * mh + f] = *reinterpret_cast<const uint16_t*>(row + hh * S + fo);
             }
         }
         __syncthreads();
