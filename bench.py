@@ -418,12 +418,14 @@ def _kernel_kind(p) -> int:
 def other_shape_rows(dev, peak_gbs: float) -> list:
     """Decode at 32K contexts in shapes outside the configurations: groups of
     16 query heads (128 q / 8 kv heads: two CTAs of 8 query heads per kv
-    head), and 2 or 4 kv heads with Lloyd-Max keys (token rows that are not
-    whole 16-byte units)."""
+    head), 2 or 4 kv heads with Lloyd-Max keys (token rows that are not
+    whole 16-byte units), and 1 or 3 kv heads with 3-bit keys (token rows
+    not 4-byte aligned: the CUDA-core stage 1)."""
     rows = []
     for preset, hq, hk in (("turboquant_k8v4", 128, 8), ("turboquant_k3v4_nc", 128, 8),
                            ("turboquant_4bit_nc", 8, 2), ("turboquant_k3v4_nc", 8, 2),
-                           ("turboquant_3bit_nc", 16, 4)):
+                           ("turboquant_3bit_nc", 16, 4), ("turboquant_k3v4_nc", 8, 1),
+                           ("turboquant_k3v4_nc", 12, 3)):
         w = wl.make("sweep", preset=preset, ctx=32768, q_heads=hq, kv_heads=hk)
         rows.append(decode_row(w, dev, peak_gbs, 30))
     return rows
