@@ -89,6 +89,22 @@ def check_decode(out, lse, ref_out, ref_lse, what=""):
     return mx, rel
 
 
+def expected_kernel_kind(preset, G, Hk):
+    """Which stage-1 kernel the library runs (1 tensor cores, 0 CUDA cores),
+    restated from its documented rule: the tensor-core stage 1 serves every
+    preset with G <= 16 (CTAs of up to 8 query heads per kv head); a CTA
+    takes the token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above
+    4) or of all Hk <= 16 heads; that part of a row must be whole 16-byte
+    units, or, when the CTA takes whole rows, a multiple of 4 bytes (copied
+    per page segment); and a two-stage ring of 32 such rows must fit in
+    ~110 KB of shared memory."""
+    slot = [196, 134, 118, 102, 70][preset]
+    hpc = 4 if (preset == 0 and Hk % 4 == 0 and Hk > 4) else Hk
+    row = hpc * slot
+    rows_ok = row % 16 == 0 or (hpc == Hk and row % 4 == 0)
+    return int(G <= 16 and hpc <= 16 and rows_ok and 2 * 32 * (row + 16) <= 110 * 1024)
+
+
 def paged_problem(orc, preset, seq_lens, Hk, bs, rng, dtype="float16", kscale=1.0, book=None):
     """Random paged cache built by the ORACLE (fp16/bf16-exact inputs).
     `book`: (centroids, midpoints) to use instead of the Lloyd-Max codebook.

@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import quantized_kv_cache_04_gb300 as tq
-from _helpers import paged_problem
+from _helpers import expected_kernel_kind, paged_problem
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,8 @@ def _decode(preset, q, cache, bt, seq_lens, Hk, bs, signs, c32, num_splits):
 
 
 @pytest.mark.parametrize("preset", [0, 1, 2, 3, 4])
-@pytest.mark.parametrize("G,Hk,bs,splits", [(4, 2, 16, 3), (4, 8, 32, 2), (16, 1, 16, 3), (2, 1, 16, 3)])
+@pytest.mark.parametrize("G,Hk,bs,splits", [(4, 2, 16, 3), (4, 8, 32, 2), (16, 1, 16, 3), (2, 1, 16, 3),
+                                             (1, 16, 16, 3)])
 def test_out_of_range_pages_give_nan_rows(orc, preset, G, Hk, bs, splits):
     dev = torch.device("cuda")
     rng = np.random.default_rng(9700 + 10 * preset + Hk)
@@ -54,12 +55,11 @@ def test_out_of_range_pages_give_nan_rows(orc, preset, G, Hk, bs, splits):
     cache = big[1:nb + 1]                      # num_blocks = nb
     assert cache.shape[0] == nb and cache.is_contiguous()
     q = torch.from_numpy(rng.normal(size=(len(seq_lens), G * Hk, 128))).to(torch.float16)
-    # the CUDA-core stage 1 serves Hk = 1 with Lloyd-Max keys (a
-    # 134/118/102/70-byte row is not 4-byte aligned); the tensor-core one the
-    # rest (rows of 4 or 8 heads' slots, or whole rows of a multiple of 4)
+    # both stage-1 kernels: one kv head with Lloyd-Max keys (rows not
+    # 4-byte aligned) and 16 kv heads of 3- or 4-bit keys (rows too large for
+    # the tensor-core ring) take the CUDA-core stage 1
     kind = tq.tq_decode_kernel_kind(preset, 128, G * Hk, Hk)
-    slot = [196, 134, 118, 102, 70][preset]
-    assert kind == (1 if (Hk * slot) % 4 == 0 else 0)
+    assert kind == expected_kernel_kind(preset, G, Hk)
 
     ref_o, ref_l = _decode(preset, q, cache, bt, seq_lens, Hk, bs, pb["signs"], pb["c32"], splits)
     assert np.all(np.isfinite(ref_o)) and np.all(np.isfinite(ref_l))

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import quantized_kv_cache_04_gb300 as tq
-from _helpers import LSE_ABS, OUT_MAX_ABS, check_decode, codebook, paged_problem, to_f32
+from _helpers import (LSE_ABS, OUT_MAX_ABS, check_decode, codebook, expected_kernel_kind, paged_problem,
+                      to_f32)
 
 pytestmark = pytest.mark.gpu
 PRESETS = [0, 1, 2, 3, 4]
@@ -51,22 +52,12 @@ CASES = [  # (G, Hk, bs, seq_lens, splits): CUDA-core and tensor-core stage 1 sh
     (2, 1, 32, [300, 45], 0),
     (4, 3, 16, [77, 400], 0),
     (4, 8, 16, [16500, 200], 0),   # a 16K-token sequence next to a short one
+    (3, 3, 32, [700, 33], 5),      # 3 kv heads: Lloyd-Max rows of 2 mod 4 bytes (CUDA cores)
 ]
 
 
 def _expected_kind(preset, G, Hk):
-    """Tensor-core stage 1 serves every preset with G <= 16 (CTAs of up to 8
-    query heads per kv head).  A CTA takes the
-    token rows of 4 kv heads (FP8 keys, Hk a multiple of 4 above 4) or of all
-    Hk <= 16 heads; that part of a row must be whole 16-byte units, or, when
-    the CTA takes whole rows, a multiple of 4 bytes (copied per page
-    segment); and a two-stage ring of 32 such rows must fit in ~110 KB of
-    shared memory."""
-    slot = [196, 134, 118, 102, 70][preset]
-    hpc = 4 if (preset == 0 and Hk % 4 == 0 and Hk > 4) else Hk
-    row = hpc * slot
-    rows_ok = row % 16 == 0 or (hpc == Hk and row % 4 == 0)
-    return int(G <= 16 and hpc <= 16 and rows_ok and 2 * 32 * (row + 16) <= 110 * 1024)
+    return expected_kernel_kind(preset, G, Hk)
 
 
 @pytest.mark.parametrize("preset", PRESETS)
