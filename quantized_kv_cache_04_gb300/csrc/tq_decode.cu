@@ -586,7 +586,7 @@ extern "C" int tq_decode_kernel_kind(int preset, int head_dim, int num_q_heads, 
     using namespace tq;
     tq_layout L;
     if (fill_layout(preset, head_dim, &L) || head_dim != kHeadDim || num_kv_heads < 1 ||
-        num_q_heads < 1 || num_q_heads % num_kv_heads)
-        return -1;
+        num_q_heads < 1 || num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > kMaxGroup)
+        return -1;                  // the shapes tq_decode_attention rejects
     return mma_stage1_supported(L, is_soa(preset), num_kv_heads, num_q_heads / num_kv_heads) ? 1 : 0;
 }

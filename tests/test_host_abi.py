@@ -153,3 +153,20 @@ def test_sparse_v_threshold_checked_on_host():
         rc = tq.tq_decode_attention_sparse_v(1, 128, 2, 8, 2, 16, 0, 1, 1, 4, 1, 4, 1, 64, 0.1, 4,
                                              1, 1, 1, 2, 0, 16, 1 << 30, tau, None)
         assert rc == _lib.TQ_ERR_INVALID_ARG
+
+
+def test_kernel_kind_follows_the_documented_rule():
+    """tq_decode_kernel_kind (host only) against the rule restated in the
+    test helpers, over every preset, 1-16 kv heads and groups of 1-20: the
+    tensor-core stage 1 for groups up to 16 whose copied row parts are whole
+    16-byte units (or whole rows of a multiple of 4 bytes) and fit its ring,
+    the CUDA-core one for the other groups up to 16, unsupported above."""
+    from _helpers import expected_kernel_kind
+    for preset in range(5):
+        for hk in range(1, 17):
+            for g in range(1, 21):
+                kind = tq.tq_decode_kernel_kind(preset, 128, g * hk, hk)
+                want = -1 if g > 16 else expected_kernel_kind(preset, g, hk)
+                assert kind == want, (preset, hk, g, kind, want)
+    assert tq.tq_decode_kernel_kind(2, 64, 8, 2) == -1          # head_dim 128 only
+    assert tq.tq_decode_kernel_kind(2, 128, 9, 2) == -1         # q heads not a multiple
