@@ -1,11 +1,12 @@
 // Decode stage 1 on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate).
 //
 // Same partials as the CUDA-core stage 1 (per split: o_s and lse_s in the
-// fp32 workspace), computed per CTA = (split, sequence) over all kv heads:
-// one warp per kv head, 32-token tiles streamed into a shared-memory ring by
-// bulk (TMA) copies of whole token rows (Hk contiguous slots each) whose
-// completion is tracked by mbarriers with bounded waits; warps only wait for
-// data, never for each other (the last warp done with a stage refills it).
+// fp32 workspace), computed per CTA = (split, sequence, kv-head group): one
+// warp per kv head, 32-token tiles streamed into a shared-memory ring by
+// bulk (TMA) copies of whole token rows (Hk contiguous slots each; FP8 keys:
+// 2-D tensor copies of 4 heads' part of each row) whose completion is
+// tracked by mbarriers with bounded waits; warps only wait for data, never
+// for each other (the last warp done with a stage refills it).
 //
 // Per tile and warp, with G query heads sharing the kv head:
 //   scores  S[t, g] = sum_d K^[t, d] Q[g, d]      A = K^ (16 tokens x 16 dims),
@@ -20,7 +21,10 @@
 // 2-bit centroids are scaled by a factor that makes them fp16-exact (no lo
 // part).  FP8 keys and integer value codes are exact in fp16.  The value
 // path uses P' = p * v_scale and adds sum_t p_t v_zero_t separately
-// (v_hat = code * scale + zero).
+// (v_hat = code * scale + zero).  With 3- or 4-bit keys and G = 8, q's lo
+// part meets only the keys' hi words, and the q fragments live in tensor
+// memory (tcgen05.st / tcgen05.ld), which leaves the shared memory to the
+// ring.
 // Centroid lookups: 3- and 4-bit keys read code pairs from a shared-memory
 // table (one 8-byte load per pair: both centroids, hi and lo); 2-bit keys
 // select bytes of register tables with PRMT.
